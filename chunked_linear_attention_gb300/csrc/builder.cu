@@ -1,0 +1,137 @@
+#include "builder.h"
+
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
+namespace ttt {
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool MapCache::get(const TensorRef& t, int box_rows, CUtensorMap* out) {
+  for (const Entry& e : entries_)
+    if (e.ptr == t.ptr && e.rows == t.rows && e.inner == t.inner && e.box_rows == box_rows) {
+      *out = e.map;
+      return true;
+    }
+  auto fn = encode_fn();
+  if (!fn || !t.bf16) return false;
+  if ((reinterpret_cast<uintptr_t>(t.ptr) & 15) != 0 || (t.inner * 2) % 16 != 0) return false;
+  Entry e;
+  e.ptr = t.ptr;
+  e.rows = t.rows;
+  e.inner = t.inner;
+  e.box_rows = box_rows;
+  cuuint64_t dims[2] = {(cuuint64_t)t.inner, (cuuint64_t)t.rows};
+  cuuint64_t strides[1] = {(cuuint64_t)t.inner * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(&e.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(t.ptr), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  entries_.push_back(e);
+  *out = e.map;
+  return true;
+}
+
+LaunchBuilder::LaunchBuilder(bool tensor_cores, MapCache* cache, int* status,
+                             unsigned long long wait_ns)
+    : tc_(tensor_cores), cache_(cache), ok_(true), status_(status), wait_ns_(wait_ns) {
+  reset();
+}
+
+void LaunchBuilder::reset() {
+  std::memset(&L_, 0, sizeof(L_));
+  nmaps_ = 0;
+  L_.status = status_;
+  L_.wait_limit_ns = wait_ns_;
+}
+
+OpDesc LaunchBuilder::op(const TensorRef& t, int mn_major, int outer_base, int z_outer,
+                         int box_rows) {
+  OpDesc o;
+  std::memset(&o, 0, sizeof(o));
+  o.mn_major = mn_major;
+  o.outer_base = outer_base;
+  o.inner_base = 0;
+  o.z_outer = z_outer;
+  o.z_div = 1;
+  const size_t es = t.bf16 ? 2 : 4;
+  o.ptr = static_cast<const char*>(t.ptr) + (size_t)outer_base * t.inner * es;
+  o.ld = t.inner;
+  o.z_stride = (long long)z_outer * t.inner;
+  if (tc_) {
+    const int box = mn_major ? 64 : box_rows;
+    int slot = -1;
+    for (int i = 0; i < nmaps_; ++i)
+      if (keys_ptr_[i] == t.ptr && keys_rows_[i] == t.rows && keys_inner_[i] == t.inner &&
+          keys_box_[i] == box)
+        slot = i;
+    if (slot < 0) {
+      if (nmaps_ >= kMaxMaps || !cache_->get(t, box, &L_.maps[nmaps_])) {
+        ok_ = false;
+        return o;
+      }
+      slot = nmaps_++;
+      keys_ptr_[slot] = t.ptr;
+      keys_rows_[slot] = t.rows;
+      keys_inner_[slot] = t.inner;
+      keys_box_[slot] = box;
+    }
+    o.map = slot;
+  }
+  return o;
+}
+
+int LaunchBuilder::choose_bn(int N, int nacc) const {
+  if (!tc_) return kSimtTile;
+  int max_bn = nacc >= 3 ? 128 : 256;
+  int best = 64;
+  long long best_area = -1;
+  for (int bn = max_bn; bn >= 64; bn -= 64) {
+    const long long area = (long long)((N + bn - 1) / bn) * bn;
+    if (best_area < 0 || area < best_area) {
+      best_area = area;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+bool LaunchBuilder::add(Problem p) {
+  if (L_.nprob >= kMaxProblems) {
+    ok_ = false;
+    return false;
+  }
+  const int bm = this->bm();
+  if (!tc_) p.bn = kSimtTile;
+  p.tiles_m = (p.M + bm - 1) / bm;
+  p.tiles_n = (p.N + p.bn - 1) / p.bn;
+  p.tile_start = L_.total_tiles;
+  L_.prob[L_.nprob++] = p;
+  L_.total_tiles += p.tiles_m * p.tiles_n * p.Z;
+  return true;
+}
+
+cudaError_t LaunchBuilder::launch(cudaStream_t stream) {
+  if (!ok_) return cudaErrorInvalidValue;
+  cudaError_t e = tc_ ? launch_umma_gemm(L_, stream) : launch_simt_gemm(L_, stream);
+  reset();
+  return e;
+}
+
+}  // namespace ttt

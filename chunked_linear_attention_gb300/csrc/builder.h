@@ -1,0 +1,71 @@
+// Host-side construction of grouped-GEMM launches: tensor views, TMA maps
+// (encoded once per call and reused), tile counts, and the launch itself on
+// the tensor-core kernel (bf16) or the fp32 SIMT kernel.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <vector>
+
+#include "gemm_desc.h"
+#include "launch.h"
+
+namespace ttt {
+
+// A dense row-major 2-D view: `rows` rows of `inner` elements.
+struct TensorRef {
+  const void* ptr;
+  int bf16;        // element type: 1 = bf16, 0 = fp32
+  long long rows;
+  int inner;
+};
+
+// TMA descriptors encoded during one call, keyed by view and box height.
+class MapCache {
+ public:
+  bool get(const TensorRef& t, int box_rows, CUtensorMap* out);
+
+ private:
+  struct Entry {
+    const void* ptr;
+    long long rows;
+    int inner;
+    int box_rows;
+    CUtensorMap map;
+  };
+  std::vector<Entry> entries_;
+};
+
+class LaunchBuilder {
+ public:
+  LaunchBuilder(bool tensor_cores, MapCache* cache, int* status, unsigned long long wait_ns);
+
+  void reset();
+  // Operand view: K-major (mn_major = 0) or MN-major; the tile origin of batch
+  // z is row outer_base + z * z_outer of `t`.
+  OpDesc op(const TensorRef& t, int mn_major, int outer_base, int z_outer, int box_rows);
+  // Tile N size for a problem with `nacc` accumulators and N columns.
+  int choose_bn(int N, int nacc) const;
+  // Fills tiles and appends.  Returns false when the launch is full.
+  bool add(Problem p);
+  cudaError_t launch(cudaStream_t stream);
+  bool ok() const { return ok_; }
+  bool tensor_cores() const { return tc_; }
+  int bm() const { return tc_ ? 128 : kSimtTile; }
+
+ private:
+  GemmLaunch L_;
+  bool tc_;
+  MapCache* cache_;
+  int nmaps_;
+  const void* keys_ptr_[kMaxMaps];
+  long long keys_rows_[kMaxMaps];
+  int keys_inner_[kMaxMaps];
+  int keys_box_[kMaxMaps];
+  bool ok_;
+  int* status_;
+  unsigned long long wait_ns_;
+};
+
+}  // namespace ttt

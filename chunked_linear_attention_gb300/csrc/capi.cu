@@ -1,0 +1,221 @@
+// The extern "C" boundary: argument validation (on the host, before anything
+// is enqueued), the device status word, and dispatch to the orchestration.
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/ttt.h"
+#include "../../include/ttt_selftest.h"
+#include "layer.h"
+
+namespace {
+
+__device__ int g_ttt_status = 0;
+
+unsigned long long g_wait_limit_ns = 2000000000ull;
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices] = {nullptr};
+
+// Device address of the status word for the current device (looked up once).
+int* status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_ttt_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const char* x = static_cast<const char*>(a);
+  const char* y = static_cast<const char*>(b);
+  return x < y + nb && y < x + na;
+}
+
+int check_layer(int B, int H, int N, int d, int m, int chunk, int io, int mode,
+                const ttt_update_rule* rule, ttt::LayerDims* D) {
+  if (!rule) return TTT_ERR_NULL;
+  if (B <= 0 || H <= 0 || N <= 0 || d <= 0 || m <= 0 || chunk <= 0) return TTT_ERR_SHAPE;
+  if (N % chunk != 0) return TTT_ERR_SHAPE;
+  if (mode < 0 || mode > 3) return TTT_ERR_ARG;
+  if (mode == TTT_BIDIRECTIONAL && chunk != N) return TTT_ERR_SHAPE;
+  if (io != TTT_F32 && io != TTT_BF16) return TTT_ERR_ARG;
+  if (rule->l2norm != 0 && rule->l2norm != 1) return TTT_ERR_ARG;
+  if (rule->muon_steps < 0 || rule->muon_steps > 64) return TTT_ERR_ARG;
+  if (!std::isfinite(rule->momentum_beta) || !std::isfinite(rule->ns_a) ||
+      !std::isfinite(rule->ns_b) || !std::isfinite(rule->ns_c))
+    return TTT_ERR_ARG;
+  if (d > 1024 || m > 1024) return TTT_ERR_UNSUPPORTED;
+  if (io == TTT_BF16 && (d % 64 != 0 || m % 64 != 0 || chunk % 128 != 0))
+    return TTT_ERR_UNSUPPORTED;
+  if ((long long)B * H * N > (1LL << 31) - 1) return TTT_ERR_UNSUPPORTED;
+  D->B = B; D->H = H; D->N = N; D->d = d; D->m = m; D->chunk = chunk;
+  D->bf16 = io == TTT_BF16;
+  D->mode = mode;
+  D->l2norm = rule->l2norm;
+  D->muon_steps = rule->muon_steps;
+  D->beta = rule->momentum_beta;
+  D->ns[0] = rule->ns_a; D->ns[1] = rule->ns_b; D->ns[2] = rule->ns_c;
+  return TTT_OK;
+}
+
+int check_lin(int B, int H, int N, int dk, int dv, int chunk, int io, int mode,
+              ttt::LinDims* D) {
+  if (B <= 0 || H <= 0 || N <= 0 || dk <= 0 || dv <= 0 || chunk <= 0) return TTT_ERR_SHAPE;
+  if (N % chunk != 0) return TTT_ERR_SHAPE;
+  if (mode < 0 || mode > 3) return TTT_ERR_ARG;
+  if (mode == TTT_BIDIRECTIONAL && chunk != N) return TTT_ERR_SHAPE;
+  if (io != TTT_F32 && io != TTT_BF16) return TTT_ERR_ARG;
+  if (io == TTT_BF16 && (dk % 64 != 0 || dv % 64 != 0 || dk > 256 || dv > 256 ||
+                         chunk % 128 != 0))
+    return TTT_ERR_UNSUPPORTED;
+  if (io == TTT_F32 && (dk > 1024 || dv > 1024)) return TTT_ERR_UNSUPPORTED;
+  if (mode == TTT_STRIDED && N / chunk > 2048) return TTT_ERR_UNSUPPORTED;
+  if ((long long)B * H * N > (1LL << 31) - 1) return TTT_ERR_UNSUPPORTED;
+  D->B = B; D->H = H; D->N = N; D->dk = dk; D->dv = dv; D->chunk = chunk;
+  D->bf16 = io == TTT_BF16;
+  D->mode = mode;
+  return TTT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ttt_status_string(int status) {
+  switch (status) {
+    case TTT_OK: return "ok";
+    case TTT_ERR_NULL: return "a required pointer is NULL";
+    case TTT_ERR_SHAPE: return "inconsistent sizes";
+    case TTT_ERR_ALIGN: return "pointer not 16-byte aligned (workspace: 256-byte)";
+    case TTT_ERR_UNSUPPORTED: return "request not supported by this build";
+    case TTT_ERR_WORKSPACE: return "workspace missing or too small";
+    case TTT_ERR_CUDA: return "CUDA runtime error";
+    case TTT_ERR_TIMEOUT: return "a kernel's bounded wait ran out";
+    case TTT_ERR_ARG: return "argument value out of range";
+    default: return "unknown status";
+  }
+}
+
+void ttt_set_wait_limit_ns(unsigned long long ns) { g_wait_limit_ns = ns ? ns : 1; }
+
+size_t ttt_layer_workspace_size(int B, int H, int N, int d_h, int m_h, int chunk, int io_dtype,
+                                int mask_mode, const ttt_update_rule* rule) {
+  ttt::LayerDims D;
+  if (check_layer(B, H, N, d_h, m_h, chunk, io_dtype, mask_mode, rule, &D) != TTT_OK) return 0;
+  return ttt::layer_workspace_bytes(D);
+}
+
+int ttt_layer_forward(const void* q, const void* k, const void* v, const float* eta,
+                      const float* W1, const float* W2, const float* W3, int w_per_batch,
+                      int B, int H, int N, int d_h, int m_h, int chunk, int io_dtype,
+                      int mask_mode, const unsigned char* update_chunks,
+                      const ttt_update_rule* rule, void* out, float* W1_final, float* W2_final,
+                      float* W3_final, float* momentum, void* workspace, size_t workspace_bytes,
+                      ttt_stream_t stream) {
+  if (!q || !k || !v || !eta || !W1 || !W2 || !W3 || !out || !W1_final || !W2_final ||
+      !W3_final || !rule)
+    return TTT_ERR_NULL;
+  ttt::LayerDims D;
+  int rc = check_layer(B, H, N, d_h, m_h, chunk, io_dtype, mask_mode, rule, &D);
+  if (rc != TTT_OK) return rc;
+  if (w_per_batch != 0 && w_per_batch != 1) return TTT_ERR_ARG;
+  if (mask_mode == TTT_STRIDED && !update_chunks) return TTT_ERR_NULL;
+  const void* ptrs[] = {q, k, v, eta, W1, W2, W3, out, W1_final, W2_final, W3_final, momentum};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return TTT_ERR_ALIGN;
+  const size_t need = ttt::layer_workspace_bytes(D);
+  if (!workspace || workspace_bytes < need) return TTT_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return TTT_ERR_ALIGN;
+  if (!w_per_batch) {
+    const size_t wbytes = (size_t)H * d_h * m_h * 4;
+    const size_t fbytes = (size_t)B * H * d_h * m_h * 4;
+    const float* ins[3] = {W1, W2, W3};
+    const float* outs[3] = {W1_final, W2_final, W3_final};
+    for (const float* i : ins)
+      for (const float* o : outs)
+        if (overlap(i, wbytes, o, fbytes)) return TTT_ERR_ARG;
+  }
+  int* st = status_ptr();
+  if (!st) return TTT_ERR_CUDA;
+  ttt::LayerArgs a;
+  a.q = q; a.k = k; a.v = v; a.eta = eta;
+  a.W[0] = W1; a.W[1] = W2; a.W[2] = W3;
+  a.w_per_batch = w_per_batch;
+  a.update_chunks = update_chunks;
+  a.out = out;
+  a.Wf[0] = W1_final; a.Wf[1] = W2_final; a.Wf[2] = W3_final;
+  a.momentum = momentum;
+  a.workspace = workspace;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  return ttt::layer_forward(a, D, st, g_wait_limit_ns);
+}
+
+size_t linattn_workspace_size(int B, int H, int N, int d_k, int d_v, int chunk, int io_dtype,
+                              int mask_mode) {
+  ttt::LinDims D;
+  if (check_lin(B, H, N, d_k, d_v, chunk, io_dtype, mask_mode, &D) != TTT_OK) return 0;
+  return ttt::linattn_workspace_bytes(D);
+}
+
+int linattn_chunked_forward(const void* q, const void* k, const void* v, const float* eta,
+                            const float* S0, int B, int H, int N, int d_k, int d_v, int chunk,
+                            int io_dtype, int mask_mode, const unsigned char* update_chunks,
+                            void* out, float* S_final, void* workspace, size_t workspace_bytes,
+                            ttt_stream_t stream) {
+  if (!q || !k || !v || !eta || !out) return TTT_ERR_NULL;
+  ttt::LinDims D;
+  int rc = check_lin(B, H, N, d_k, d_v, chunk, io_dtype, mask_mode, &D);
+  if (rc != TTT_OK) return rc;
+  if (mask_mode == TTT_STRIDED && !update_chunks) return TTT_ERR_NULL;
+  const void* ptrs[] = {q, k, v, eta, S0, out, S_final};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return TTT_ERR_ALIGN;
+  const size_t need = ttt::linattn_workspace_bytes(D);
+  if (!workspace || workspace_bytes < need) return TTT_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return TTT_ERR_ALIGN;
+  int* st = status_ptr();
+  if (!st) return TTT_ERR_CUDA;
+  ttt::LinArgs a;
+  a.q = q; a.k = k; a.v = v; a.eta = eta; a.S0 = S0;
+  a.update_chunks = update_chunks;
+  a.out = out;
+  a.S_final = S_final;
+  a.workspace = workspace;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  return ttt::linattn_forward(a, D, st, g_wait_limit_ns);
+}
+
+int ttt_device_status(ttt_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return TTT_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_ttt_status, sizeof(int)) != cudaSuccess) return TTT_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_ttt_status, &zero, sizeof(int)) != cudaSuccess) return TTT_ERR_CUDA;
+  return v;
+}
+
+int ttt_selftest_gemm(const void* A, const void* B, float* D, int Z, int M, int N, int K,
+                      int a_mn_major, int b_mn_major, int dtype, int tile_n,
+                      ttt_stream_t stream) {
+  if (!A || !B || !D) return TTT_ERR_NULL;
+  if (Z <= 0 || M <= 0 || N <= 0 || K <= 0) return TTT_ERR_SHAPE;
+  if (dtype != TTT_F32 && dtype != TTT_BF16) return TTT_ERR_ARG;
+  if (dtype == TTT_BF16) {
+    if (M % 64 || N % 64 || K % 64) return TTT_ERR_UNSUPPORTED;
+    if (tile_n != 64 && tile_n != 128 && tile_n != 192 && tile_n != 256) return TTT_ERR_ARG;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(D)) return TTT_ERR_ALIGN;
+  }
+  int* st = status_ptr();
+  if (!st) return TTT_ERR_CUDA;
+  return ttt::selftest_gemm(A, B, D, Z, M, N, K, a_mn_major ? 1 : 0, b_mn_major ? 1 : 0,
+                            dtype == TTT_BF16, tile_n, reinterpret_cast<cudaStream_t>(stream), st,
+                            g_wait_limit_ns);
+}
+
+}  // extern "C"

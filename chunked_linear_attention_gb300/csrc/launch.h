@@ -1,0 +1,41 @@
+// Host-side launchers of the library's kernels (one definition per .cu file).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "gemm_desc.h"
+
+namespace ttt {
+
+// Dynamic shared memory of the tensor-core GEMM: the whole 227 KB, so one CTA
+// owns an SM and its TMEM (no allocation contention).
+constexpr int kUmmaSmemBytes = 227 * 1024;
+constexpr int kSimtTile = 64;
+
+cudaError_t launch_umma_gemm(const GemmLaunch& L, cudaStream_t stream);
+cudaError_t launch_simt_gemm(const GemmLaunch& L, cudaStream_t stream);
+
+// ---- elementwise / reduction kernels (aux_kernels.cu)
+
+// One fast-weight matrix family (W1, W2 or W3) for the update steps.
+struct MatSet {
+  const float* init;      // initial weights [H or B*H][rows*cols]
+  int init_per_batch;     // 1: init indexed by b*H+h, 0: by h
+  float* master;          // fp32 state [B*H][rows*cols] (the caller's W_final)
+  void* work;             // operand copy [B*H][rows*cols] (bf16) or NULL
+  const float* update;    // U [B*H][rows*cols] subtracted by normalize
+  int rows, cols;
+};
+
+// master = init (broadcast over the batch), work = bf16(master).
+cudaError_t launch_init_weights(const MatSet& m, int B, int H, cudaStream_t stream);
+
+// master = RowNorm(master - update) (or master - update), work = bf16(master);
+// clears `clear_n` floats at `clear` afterwards (Newton-Schulz norms).
+cudaError_t launch_update_normalize(const MatSet* sets, int nsets, int BH, int l2norm,
+                                    float* clear, int clear_n, cudaStream_t stream);
+
+// dst[i] = src[i] (float), for i < n; src NULL -> zeros.
+cudaError_t launch_copy_f32(float* dst, const float* src, long long n, cudaStream_t stream);
+
+}  // namespace ttt

@@ -1,0 +1,67 @@
+// Internal interface between the C ABI (capi.cu) and the host orchestration
+// of the TTT layer (layer.cu) and chunked linear attention (linattn.cu).
+// Arguments reaching these functions have been validated.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+namespace ttt {
+
+struct LayerDims {
+  int B, H, N, d, m, chunk;
+  bool bf16;
+  int mode;
+  int l2norm;
+  int muon_steps;
+  float beta;
+  float ns[3];
+};
+
+struct LayerArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* eta;
+  const float* W[3];   // W1, W2, W3
+  int w_per_batch;
+  const unsigned char* update_chunks;  // host
+  void* out;
+  float* Wf[3];        // W1_final, W2_final, W3_final
+  float* momentum;     // [3][B*H][d*m] (M1, M2, M3) or NULL
+  void* workspace;
+  cudaStream_t stream;
+};
+
+size_t layer_workspace_bytes(const LayerDims& D);
+// Returns a ttt_status code.
+int layer_forward(const LayerArgs& a, const LayerDims& D, int* status, unsigned long long wait_ns);
+
+struct LinDims {
+  int B, H, N, dk, dv, chunk;
+  bool bf16;
+  int mode;
+};
+
+struct LinArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* eta;
+  const float* S0;
+  const unsigned char* update_chunks;  // host
+  void* out;
+  float* S_final;
+  void* workspace;
+  cudaStream_t stream;
+};
+
+size_t linattn_workspace_bytes(const LinDims& D);
+int linattn_forward(const LinArgs& a, const LinDims& D, int* status, unsigned long long wait_ns);
+
+// Self-test GEMM (capi.cu) uses the builder directly.
+int selftest_gemm(const void* A, const void* Bp, float* Dp, int Z, int M, int N, int K, int a_mn,
+                  int b_mn, bool bf16, int tile_n, cudaStream_t stream, int* status,
+                  unsigned long long wait_ns);
+
+}  // namespace ttt

@@ -1,0 +1,168 @@
+// Host orchestration of chunked linear attention ("Test-Time Training with KV
+// Binding Is Secretly Linear Attention", Thm 5.2 and App. H with alpha = 0;
+// the causal state update of "From Linear Attention to Test-Time Training").
+//
+// The state after chunk c is S0 + sum over visible chunks of V~_c^T K_c with
+// V~ = eta * V.  The chunk sums are independent, so the scan is three
+// parallel passes over all (batch, head, chunk) at once:
+//   1. V~ = eta * V (bf16 rows), then per (batch, head, chunk, split) the
+//      partial state V~_split^T K_split on the tensor cores (K = split tokens)
+//   2. a prefix over chunks: the state each chunk reads (bf16 operand copy)
+//      and the final fp32 state
+//   3. O_c = Q_c S_c^T on the tensor cores, all chunks in one launch.
+#include <algorithm>
+#include <cstring>
+
+#include "builder.h"
+#include "layer.h"
+#include "linattn_kernels.h"
+
+namespace ttt {
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+int choose_splits(const LinDims& D, int tiles_per_z) {
+  const long long pairs = (long long)D.B * D.H * (D.N / D.chunk);
+  int splits = 1;
+  while (pairs * splits * tiles_per_z < 2 * 152) {
+    const int next = splits * 2;
+    if (D.chunk % next != 0) break;
+    const int len = D.chunk / next;
+    if (len < 256 || len % 64 != 0) break;
+    splits = next;
+  }
+  return splits;
+}
+
+struct LinWs {
+  void* Vt;
+  float* partials;
+  void* Sread;
+  int splits;
+};
+
+size_t lin_layout(const LinDims& D, LinWs* w, char* base) {
+  const size_t BH = (size_t)D.B * D.H;
+  const size_t nc = D.N / D.chunk;
+  const size_t es = D.bf16 ? 2 : 4;
+  const int tiles = D.bf16 ? ((D.dv + 127) / 128) * ((D.dk + 127) / 128)
+                           : ((D.dv + 63) / 64) * ((D.dk + 63) / 64);
+  const int splits = choose_splits(D, tiles);
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> char* {
+    char* p = base ? base + off : nullptr;
+    off += align_up(bytes);
+    return p;
+  };
+  LinWs tmp;
+  LinWs& o = w ? *w : tmp;
+  o.splits = splits;
+  o.Vt = take(BH * D.N * D.dv * es);
+  o.partials = reinterpret_cast<float*>(take(BH * nc * splits * D.dv * D.dk * 4));
+  o.Sread = take(BH * nc * D.dv * D.dk * es);
+  return off;
+}
+
+Problem prob0(int M, int N, int K, int Z, int nacc, int bn) {
+  Problem p;
+  std::memset(&p, 0, sizeof(p));
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.Z = Z;
+  p.nacc = nacc;
+  p.bn = bn;
+  p.epi.z_div = 1;
+  return p;
+}
+
+}  // namespace
+
+size_t linattn_workspace_bytes(const LinDims& D) { return lin_layout(D, nullptr, nullptr); }
+
+int linattn_forward(const LinArgs& a, const LinDims& D, int* status, unsigned long long wait_ns) {
+  LinWs w;
+  lin_layout(D, &w, static_cast<char*>(a.workspace));
+  cudaStream_t st = a.stream;
+  const bool tc = D.bf16;
+  const int BH = D.B * D.H, N = D.N, dk = D.dk, dv = D.dv, b = D.chunk;
+  const int nc = N / b;
+  const int splits = w.splits, slen = b / splits;
+  const int wb16 = tc ? 1 : 0;
+
+  UpdateFlags flags;
+  std::memset(&flags, 0, sizeof(flags));
+  flags.all = D.mode != 3;
+  if (D.mode == 3)
+    for (int c = 0; c < nc; ++c)
+      if (a.update_chunks[c]) flags.bits[c >> 5] |= 1u << (c & 31);
+
+  if (launch_scale_rows(a.v, a.eta, w.Vt, (long long)BH * N, dv, tc, st) != cudaSuccess)
+    return -6;
+
+  MapCache cache;
+  LaunchBuilder LB(tc, &cache, status, wait_ns);
+  const int BM = LB.bm();
+  TensorRef TVt{w.Vt, wb16, (long long)BH * N, dv};
+  TensorRef Tk{a.k, wb16, (long long)BH * N, dk};
+  TensorRef Tq{a.q, wb16, (long long)BH * N, dk};
+  TensorRef TS{w.Sread, wb16, (long long)BH * nc * dv, dk};
+
+  {  // partial states
+    const int bn = LB.choose_bn(dk, 1);
+    Problem p = prob0(dv, dk, slen, BH * nc * splits, 1, bn);
+    p.a[0] = LB.op(TVt, 1, 0, slen, 64);
+    p.b[0] = LB.op(Tk, 1, 0, slen, 64);
+    p.epi.kind = EPI_STORE_F32;
+    p.epi.out[0] = w.partials;
+    p.epi.out_ld = dk;
+    p.epi.out_z = (long long)dv * dk;
+    LB.add(p);
+    if (!LB.ok()) return -4;
+    if (LB.launch(st) != cudaSuccess) return -6;
+  }
+  if (launch_linattn_prefix(w.partials, a.S0, w.Sread, a.S_final, BH, nc, splits, dv * dk,
+                            D.mode == 0, flags, tc, st) != cudaSuccess)
+    return -6;
+  {  // outputs
+    const int bn = LB.choose_bn(dv, 1);
+    Problem p = prob0(b, dv, dk, BH * nc, 1, bn);
+    p.a[0] = LB.op(Tq, 0, 0, b, BM);
+    p.b[0] = LB.op(TS, 0, 0, dv, bn);
+    p.epi.kind = EPI_OUT;
+    p.epi.out[0] = a.out;
+    p.epi.out_ld = dv;
+    p.epi.out_z = (long long)b * dv;
+    LB.add(p);
+    if (!LB.ok()) return -4;
+    if (LB.launch(st) != cudaSuccess) return -6;
+  }
+  return 0;
+}
+
+int selftest_gemm(const void* A, const void* Bp, float* Dp, int Z, int M, int N, int K, int a_mn,
+                  int b_mn, bool bf16, int tile_n, cudaStream_t stream, int* status,
+                  unsigned long long wait_ns) {
+  MapCache cache;
+  LaunchBuilder LB(bf16, &cache, status, wait_ns);
+  const int wb16 = bf16 ? 1 : 0;
+  const int bn = bf16 ? tile_n : kSimtTile;
+  // A: K-major [Z*M, K] or MN-major [Z*K, M]; B: K-major [Z*N, K] or [Z*K, N]
+  TensorRef TA = a_mn ? TensorRef{A, wb16, (long long)Z * K, M} : TensorRef{A, wb16, (long long)Z * M, K};
+  TensorRef TB = b_mn ? TensorRef{Bp, wb16, (long long)Z * K, N} : TensorRef{Bp, wb16, (long long)Z * N, K};
+  Problem p = prob0(M, N, K, Z, 1, bn);
+  p.a[0] = LB.op(TA, a_mn, 0, a_mn ? K : M, LB.bm());
+  p.b[0] = LB.op(TB, b_mn, 0, b_mn ? K : N, bn);
+  p.epi.kind = EPI_STORE_F32;
+  p.epi.out[0] = Dp;
+  p.epi.out_ld = N;
+  p.epi.out_z = (long long)M * N;
+  LB.add(p);
+  if (!LB.ok()) return -4;
+  return LB.launch(stream) == cudaSuccess ? 0 : -6;
+}
+
+}  // namespace ttt

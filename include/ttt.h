@@ -1,0 +1,178 @@
+/*
+ * ttt.h - C ABI of the GB300 (sm_103a) large-chunk TTT-KVB layer and its
+ * chunked linear-attention reduction.
+ *
+ * The operation (from "5.2.1 LaCT and TTT-E2E", eqs (2)-(6) and (10), and
+ * "Test-Time Training with KV Binding Is Secretly Linear Attention", sec. 5.3,
+ * 6.1, App. E, H): each (batch, head) carries a bias-free SwiGLU fast-weight
+ * net f_W(x) = W2 [SiLU(W1 x) o (W3 x)].  The sequence is cut into chunks of
+ * `chunk` tokens.  Per chunk the layer
+ *   (apply)  o_i = f_W(q_i) for every query of the chunk, and
+ *   (update) g = grad_W sum_i eta_i * (-f_W(k_i)^T v_i)   (summed, no 1/b),
+ *            M <- beta M + g, U = Muon(M) (Newton-Schulz) or M,
+ *            W <- L2-Normalize(W - U) (rows to unit norm over the input dim),
+ * in the order the mask mode sets.  For a linear fast weight the layer is the
+ * chunked linear attention computed by linattn_chunked_forward.
+ *
+ * Conventions for every entry point:
+ *   - All pointers are DEVICE pointers (cudaMalloc'd or otherwise
+ *     device-accessible) unless the argument says "host".  The caller owns
+ *     every buffer; the library allocates nothing on the call path.
+ *   - Tensors are dense row-major with the shapes given per argument.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream).  Argument errors are found on the host and returned
+ *     before anything is enqueued.  Failures detected by a kernel (a bounded
+ *     wait that ran out) are recorded in a device status word that
+ *     ttt_device_status() reads.
+ *   - Inputs are read-only; q and k may alias (the "replace Q with K" use).
+ *   - bf16 I/O computes with bf16 tensor-core operands and fp32 accumulation
+ *     and fp32 fast-weight state; fp32 I/O computes in fp32 throughout (no
+ *     TF32).  There is no CPU fallback.
+ */
+#ifndef TTT_GB300_TTT_H
+#define TTT_GB300_TTT_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* ttt_stream_t; /* a cudaStream_t */
+
+typedef enum {
+  TTT_OK = 0,
+  TTT_ERR_NULL = -1,        /* a required pointer is NULL */
+  TTT_ERR_SHAPE = -2,       /* sizes inconsistent (e.g. N % chunk != 0) */
+  TTT_ERR_ALIGN = -3,       /* a pointer is not 16-byte aligned */
+  TTT_ERR_UNSUPPORTED = -4, /* valid request this build does not implement */
+  TTT_ERR_WORKSPACE = -5,   /* workspace NULL or smaller than the query says */
+  TTT_ERR_CUDA = -6,        /* a CUDA runtime call failed (no device, launch) */
+  TTT_ERR_TIMEOUT = -7,     /* a kernel's bounded wait ran out (device word) */
+  TTT_ERR_ARG = -8          /* an argument value is out of range */
+} ttt_status;
+
+typedef enum { TTT_F32 = 0, TTT_BF16 = 1 } ttt_dtype;
+
+/* Order of apply and update per chunk ("5.2.1 LaCT and TTT-E2E", sec. 1.1 and
+ * eq (10)).
+ *   TTT_APPLY_THEN_UPDATE: chunk c is read with the state after chunks
+ *                          0..c-1, then chunk c updates it (causal LM).
+ *   TTT_BLOCK_CAUSAL:      chunk c updates first, then is read (block mask).
+ *   TTT_BIDIRECTIONAL:     one chunk covering the sequence (chunk == N),
+ *                          update then apply (full attention).
+ *   TTT_STRIDED:           update (then apply) only on chunks flagged in
+ *                          update_chunks; apply on every chunk. */
+typedef enum {
+  TTT_APPLY_THEN_UPDATE = 0,
+  TTT_BLOCK_CAUSAL = 1,
+  TTT_BIDIRECTIONAL = 2,
+  TTT_STRIDED = 3
+} ttt_mask_mode;
+
+/* Weight-update rule ("5.2.1 LaCT and TTT-E2E", eqs (5), (6) and the
+ * momentum sentence after eq (6)).
+ *   l2norm        : 1 = L2-Normalize every row of W1, W2, W3 after W - U.
+ *   muon_steps    : Newton-Schulz steps of Muon(M); 0 = U is M itself.
+ *   momentum_beta : M <- beta M + g; 0 = no momentum (M = g).
+ *   ns_a/ns_b/ns_c: Newton-Schulz coefficients X <- aX + b(XX^T)X + c(XX^T)^2X
+ *                   (the Muon quintic is 3.4445, -4.7750, 2.0315).
+ * Muon first scales M to unit Frobenius norm (eps 1e-7) and transposes a
+ * matrix with more rows than columns. */
+typedef struct {
+  int l2norm;
+  int muon_steps;
+  float momentum_beta;
+  float ns_a, ns_b, ns_c;
+} ttt_update_rule;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* ttt_status_string(int status);
+
+/* Bytes of device workspace ttt_layer_forward needs for these arguments
+ * (0 if the arguments are invalid).  rule may not be NULL. */
+size_t ttt_layer_workspace_size(int B, int H, int N, int d_h, int m_h, int chunk,
+                                int io_dtype, int mask_mode,
+                                const ttt_update_rule* rule);
+
+/* The LaCT TTT layer forward over a whole sequence.
+ *
+ *   q, k, v     [B, H, N, d_h] in io_dtype (k may alias q).
+ *   eta         [B, H, N] fp32: per-token learning rate eta_i (eq 2); any
+ *               sign (negative eta is gradient ascent).
+ *   W1, W3      fp32 initial fast weights [H, m_h, d_h] (w_per_batch = 0,
+ *               shared over the batch) or [B, H, m_h, d_h] (w_per_batch = 1).
+ *   W2          fp32 [H, d_h, m_h] or [B, H, d_h, m_h] likewise.
+ *   chunk       tokens per chunk; N % chunk == 0; BIDIRECTIONAL needs
+ *               chunk == N.
+ *   update_chunks  HOST array of N/chunk bytes (nonzero = update on that
+ *               chunk); read only for TTT_STRIDED, may be NULL otherwise.
+ *   rule        HOST pointer to the update rule.
+ *   out         [B, H, N, d_h] in io_dtype: o_i = f_W(q_i).
+ *   W1_final, W3_final  fp32 [B, H, m_h, d_h]; W2_final fp32 [B, H, d_h, m_h]:
+ *               the fast weights after the last chunk.  They hold the running
+ *               state during the call; they may alias W1/W2/W3 only when
+ *               w_per_batch = 1.
+ *   momentum    NULL, or fp32 [3][B][H][m_h*d_h] in the order M1, M2, M3
+ *               (M2 stored [d_h, m_h]): read as the initial momentum and
+ *               overwritten with the final one.  NULL = zero start, discarded.
+ *   workspace   device scratch of at least ttt_layer_workspace_size() bytes,
+ *               256-byte aligned, not shared with a concurrent call.
+ *
+ * Supported: io_dtype TTT_BF16 with d_h, m_h multiples of 64 (<= 1024) and
+ * chunk a multiple of 128; io_dtype TTT_F32 with d_h, m_h <= 1024.  Other
+ * requests return TTT_ERR_UNSUPPORTED.  Device pointers must be 16-byte
+ * aligned.  Returns TTT_OK when the work was enqueued. */
+int ttt_layer_forward(const void* q, const void* k, const void* v, const float* eta,
+                      const float* W1, const float* W2, const float* W3, int w_per_batch,
+                      int B, int H, int N, int d_h, int m_h, int chunk, int io_dtype,
+                      int mask_mode, const unsigned char* update_chunks,
+                      const ttt_update_rule* rule,
+                      void* out, float* W1_final, float* W2_final, float* W3_final,
+                      float* momentum, void* workspace, size_t workspace_bytes,
+                      ttt_stream_t stream);
+
+/* Bytes of device workspace linattn_chunked_forward needs (0 if invalid). */
+size_t linattn_workspace_size(int B, int H, int N, int d_k, int d_v, int chunk,
+                              int io_dtype, int mask_mode);
+
+/* Chunked linear attention: the TTT layer with a linear fast weight
+ * f_S(x) = S x, S0 initial state, dot-product loss and no normalisation
+ * ("Test-Time Training with KV Binding Is Secretly Linear Attention",
+ * Thm 5.2, sec. 6.1 step 6, App. H with alpha = 0).  Per chunk
+ *   S <- S + sum_i eta_i v_i k_i^T   and   o_i = S q_i,
+ * in the order the mask mode sets, so with S0 = 0 and block-causal order
+ * o_i = sum_{chunk(j) <= chunk(i)} eta_j (q_i . k_j) v_j.
+ *
+ *   q, k        [B, H, N, d_k] in io_dtype;  v [B, H, N, d_v] in io_dtype.
+ *   eta         [B, H, N] fp32.
+ *   S0          fp32 [B, H, d_v, d_k] initial state, or NULL for zeros.
+ *   update_chunks  HOST flags for TTT_STRIDED (else may be NULL).
+ *   out         [B, H, N, d_v] in io_dtype.
+ *   S_final     fp32 [B, H, d_v, d_k] state after the last chunk (may be NULL).
+ *   workspace   at least linattn_workspace_size() bytes, 256-byte aligned.
+ *
+ * Supported: io_dtype TTT_BF16 with d_k, d_v multiples of 64 (<= 256) and
+ * chunk a multiple of 128; io_dtype TTT_F32 with d_k, d_v <= 1024. */
+int linattn_chunked_forward(const void* q, const void* k, const void* v, const float* eta,
+                            const float* S0, int B, int H, int N, int d_k, int d_v,
+                            int chunk, int io_dtype, int mask_mode,
+                            const unsigned char* update_chunks,
+                            void* out, float* S_final,
+                            void* workspace, size_t workspace_bytes, ttt_stream_t stream);
+
+/* Synchronises `stream`, then returns and clears the device status word:
+ * TTT_OK, TTT_ERR_TIMEOUT if a kernel's bounded wait ran out since the last
+ * call, or TTT_ERR_CUDA if the synchronisation itself failed. */
+int ttt_device_status(ttt_stream_t stream);
+
+/* Sets the bounded-wait limit of the library's kernels in nanoseconds
+ * (default 2e9).  Takes effect for launches enqueued after the call. */
+void ttt_set_wait_limit_ns(unsigned long long ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TTT_GB300_TTT_H */

@@ -1,0 +1,272 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerances are the ones the method's benchmark table states: max relative
+error (max|x - r| / max|r|) <= 1e-4 for the fp32 path; relative L2 error
+<= 2e-2 for bf16 (<= 3e-2 with Muon), per output tensor (out and each final
+fast-weight matrix).
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import ttt_oracle as O
+from tests.gpu_util import assert_status_ok, f64, lib, max_rel, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+F32_MAX_REL = 1e-4
+BF16_REL_L2 = 2e-2
+BF16_MUON_REL_L2 = 3e-2
+DEV = "cuda:0"
+
+
+# ---------------------------------------------------------------------------
+# the GEMM building block against a plain fp32 product
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (1, 0), (0, 1), (1, 1)])
+@pytest.mark.parametrize("tile_n", [64, 128, 192, 256])
+def test_selftest_gemm_bf16(a_mn, b_mn, tile_n):
+    cla = lib()
+    g = torch.Generator(device="cpu").manual_seed(7)
+    Z, M, N, K = 2, 256, 384, 192
+    A = torch.randn((Z, K, M) if a_mn else (Z, M, K), generator=g).to(torch.bfloat16)
+    B = torch.randn((Z, K, N) if b_mn else (Z, N, K), generator=g).to(torch.bfloat16)
+    D = cla.selftest_gemm(A.to(DEV), B.to(DEV), bool(a_mn), bool(b_mn), tile_n)
+    torch.cuda.synchronize()
+    assert_status_ok(cla)
+    Af = A.double().transpose(1, 2) if a_mn else A.double()
+    Bf = B.double() if b_mn else B.double().transpose(1, 2)
+    ref = torch.bmm(Af, Bf).numpy()
+    assert rel_l2(f64(D), ref) < 1e-5
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (1, 1)])
+def test_selftest_gemm_f32(a_mn, b_mn):
+    cla = lib()
+    g = torch.Generator(device="cpu").manual_seed(8)
+    Z, M, N, K = 3, 70, 45, 33
+    A = torch.randn((Z, K, M) if a_mn else (Z, M, K), generator=g)
+    B = torch.randn((Z, K, N) if b_mn else (Z, N, K), generator=g)
+    D = cla.selftest_gemm(A.to(DEV), B.to(DEV), bool(a_mn), bool(b_mn))
+    torch.cuda.synchronize()
+    Af = A.double().transpose(1, 2) if a_mn else A.double()
+    Bf = B.double() if b_mn else B.double().transpose(1, 2)
+    assert max_rel(f64(D), torch.bmm(Af, Bf).numpy()) < 1e-5
+
+
+# ---------------------------------------------------------------------------
+# TTT layer
+
+def run_layer(cla, wl, q, k, v, eta, W1, W2, W3, momentum=None):
+    rule = cla.update_rule(l2norm=wl.l2norm, muon_steps=wl.muon_steps,
+                           momentum_beta=wl.momentum_beta)
+    res = cla.ttt_layer_forward(q.to(DEV), k.to(DEV), v.to(DEV), eta.to(DEV), W1.to(DEV),
+                                W2.to(DEV), W3.to(DEV), wl.chunk, wl.mode, rule,
+                                update_chunks=wl.update_chunks, momentum=momentum)
+    torch.cuda.synchronize()
+    assert_status_ok(cla)
+    return [f64(t) for t in res]
+
+
+def run_oracle(wl, q, k, v, eta, W1, W2, W3, n_chunks=None, momentum=None):
+    return O.ttt_layer_forward(f64(q), f64(k), f64(v), f64(eta), f64(W1), f64(W2), f64(W3),
+                               wl.chunk, wl.mode, update_chunks=wl.update_chunks,
+                               l2norm=wl.l2norm, muon_steps=wl.muon_steps,
+                               momentum_beta=wl.momentum_beta, momentum=momentum,
+                               n_chunks=n_chunks)
+
+
+def test_layer_tiny_fp32():
+    """The tiny fp32 workload exactly as specified: max rel error <= 1e-4."""
+    cla = lib()
+    wl = W.TINY_F32
+    inp = W.layer_inputs(wl)
+    got = run_layer(cla, wl, *inp)
+    ref = run_oracle(wl, *inp)
+    for g_, r_ in zip(got, ref[:4]):
+        assert max_rel(g_, r_) <= F32_MAX_REL
+
+
+FP32_CASES = [
+    dict(mode=W.APPLY_THEN_UPDATE, chunk=16, N=64, d_h=24, m_h=40, muon_steps=3, momentum_beta=0.9),
+    dict(mode=W.BLOCK_CAUSAL, chunk=32, N=128, d_h=33, m_h=17, muon_steps=0, momentum_beta=0.5),
+    dict(mode=W.BIDIRECTIONAL, chunk=96, N=96, d_h=16, m_h=16, muon_steps=2, momentum_beta=0.0),
+    dict(mode=W.STRIDED, chunk=16, N=96, d_h=20, m_h=36, muon_steps=1, momentum_beta=0.0,
+         update_chunks=(1, 0, 1, 0, 0, 1)),
+    dict(mode=W.APPLY_THEN_UPDATE, chunk=8, N=40, d_h=8, m_h=8, l2norm=False),
+]
+
+
+@pytest.mark.parametrize("case", FP32_CASES)
+def test_layer_fp32_variants(case):
+    cla = lib()
+    wl = dataclasses.replace(W.TINY_F32, B=2, H=2, **case)
+    inp = W.layer_inputs(wl)
+    got = run_layer(cla, wl, *inp)
+    ref = run_oracle(wl, *inp)
+    for g_, r_ in zip(got, ref[:4]):
+        assert max_rel(g_, r_) <= F32_MAX_REL
+
+
+BF16_CASES = [
+    dict(mode=W.APPLY_THEN_UPDATE, chunk=128, N=512, d_h=128, m_h=128),
+    dict(mode=W.APPLY_THEN_UPDATE, chunk=128, N=512, d_h=128, m_h=128, muon_steps=3,
+         momentum_beta=0.9),
+    dict(mode=W.BLOCK_CAUSAL, chunk=256, N=1024, d_h=128, m_h=192, momentum_beta=0.5),
+    dict(mode=W.BLOCK_CAUSAL, chunk=128, N=512, d_h=192, m_h=128, muon_steps=2),
+    dict(mode=W.BLOCK_CAUSAL, chunk=128, N=384, d_h=128, m_h=320, muon_steps=2,
+         momentum_beta=0.9),
+    dict(mode=W.BIDIRECTIONAL, chunk=512, N=512, d_h=128, m_h=128, muon_steps=1),
+    dict(mode=W.STRIDED, chunk=128, N=1024, d_h=128, m_h=256,
+         update_chunks=(1, 0, 1, 1, 0, 0, 0, 0)),
+    dict(mode=W.APPLY_THEN_UPDATE, chunk=128, N=512, d_h=64, m_h=64, l2norm=False),
+]
+
+
+@pytest.mark.parametrize("case", BF16_CASES)
+def test_layer_bf16_variants(case):
+    cla = lib()
+    wl = dataclasses.replace(W.LM_760M, B=2, H=2, muon_steps=0, momentum_beta=0.0,
+                             l2_normed_k=False, **case)
+    inp = W.layer_inputs(wl)
+    got = run_layer(cla, wl, *inp)
+    ref = run_oracle(wl, *inp)
+    tol = BF16_MUON_REL_L2 if wl.muon_steps else BF16_REL_L2
+    errs = [rel_l2(g_, r_) for g_, r_ in zip(got, ref[:4])]
+    assert max(errs) <= tol, errs
+
+
+def test_layer_bf16_per_batch_weights_and_momentum_carry():
+    """Per-batch initial weights, and a sequence split in two calls with the
+    final weights and momentum fed back equals the oracle's single pass."""
+    cla = lib()
+    wl = dataclasses.replace(W.LM_760M, B=2, H=2, N=512, d_h=128, m_h=128, chunk=128,
+                             muon_steps=2, momentum_beta=0.9)
+    q, k, v, eta, W1, W2, W3 = W.layer_inputs(wl)
+    W1b, W2b, W3b = (x.unsqueeze(0).repeat(2, 1, 1, 1).contiguous() for x in (W1, W2, W3))
+    W1b[1] *= 1.5
+    ref = run_oracle(wl, q, k, v, eta, W1b, W2b, W3b)
+    half = wl.N // 2
+    wh = dataclasses.replace(wl, N=half)
+    mom = torch.zeros(3 * 2 * 2 * 128 * 128, device=DEV)
+    sl = lambda t: t[..., :half, :].contiguous()
+    o1, A1, A2, A3 = run_layer(cla, wh, sl(q), sl(k), sl(v), eta[..., :half].contiguous(),
+                               W1b, W2b, W3b, momentum=mom)
+    sr = lambda t: t[..., half:, :].contiguous()
+    o2, B1, B2, B3 = run_layer(cla, wh, sr(q), sr(k), sr(v), eta[..., half:].contiguous(),
+                               torch.from_numpy(A1).float(), torch.from_numpy(A2).float(),
+                               torch.from_numpy(A3).float(), momentum=mom)
+    out = np.concatenate([o1, o2], axis=2)
+    errs = [rel_l2(out, ref[0]), rel_l2(B1, ref[1]), rel_l2(B2, ref[2]), rel_l2(B3, ref[3])]
+    assert max(errs) <= BF16_MUON_REL_L2, errs
+
+
+def test_layer_replace_q_with_k_and_gradient_ascent():
+    cla = lib()
+    wl = dataclasses.replace(W.LM_760M, B=1, H=2, N=512, d_h=128, m_h=128, chunk=128,
+                             muon_steps=0, momentum_beta=0.0)
+    q, k, v, eta, W1, W2, W3 = W.layer_inputs(wl)
+    for qq, ee in ((k, eta), (q, -eta)):
+        got = run_layer(cla, wl, qq, k, v, ee.contiguous(), W1, W2, W3)
+        ref = run_oracle(wl, qq, k, v, ee, W1, W2, W3)
+        errs = [rel_l2(g_, r_) for g_, r_ in zip(got, ref[:4])]
+        assert max(errs) <= BF16_REL_L2, errs
+
+
+# ---------------------------------------------------------------------------
+# chunked linear attention
+
+LIN_CASES = [
+    dict(mode=W.BLOCK_CAUSAL, chunk=256, N=1024),
+    dict(mode=W.APPLY_THEN_UPDATE, chunk=128, N=1024),
+    dict(mode=W.BIDIRECTIONAL, chunk=1024, N=1024),
+    dict(mode=W.STRIDED, chunk=128, N=1024, update_chunks=(0, 1, 1, 0, 1, 0, 0, 1)),
+    dict(mode=W.BLOCK_CAUSAL, chunk=256, N=768, d_k=64, d_v=192),
+]
+
+
+@pytest.mark.parametrize("case", LIN_CASES)
+@pytest.mark.parametrize("with_state", [False, True])
+def test_linattn_bf16(case, with_state):
+    cla = lib()
+    wl = dataclasses.replace(W.LINATTN_C2, B=2, H=2, **case)
+    q, k, v, eta, S0 = W.linattn_inputs(wl, with_state=with_state)
+    o, S = cla.linattn_chunked_forward(q.to(DEV), k.to(DEV), v.to(DEV), eta.to(DEV), wl.chunk,
+                                       wl.mode, S0=None if S0 is None else S0.to(DEV),
+                                       update_chunks=wl.update_chunks)
+    torch.cuda.synchronize()
+    assert_status_ok(cla)
+    ro, rS = O.linattn_chunked_forward(f64(q), f64(k), f64(v), f64(eta),
+                                       None if S0 is None else f64(S0), wl.chunk, wl.mode,
+                                       wl.update_chunks)
+    assert rel_l2(f64(o), ro) <= BF16_REL_L2
+    assert rel_l2(f64(S), rS) <= BF16_REL_L2
+
+
+@pytest.mark.parametrize("mode", [W.APPLY_THEN_UPDATE, W.BLOCK_CAUSAL])
+def test_linattn_fp32(mode):
+    cla = lib()
+    wl = dataclasses.replace(W.LINATTN_C2, B=2, H=3, N=200, d_k=24, d_v=40, chunk=40, mode=mode,
+                             io_dtype="f32")
+    q, k, v, eta, S0 = W.linattn_inputs(wl, with_state=True)
+    o, S = cla.linattn_chunked_forward(q.to(DEV), k.to(DEV), v.to(DEV), eta.to(DEV), wl.chunk,
+                                       wl.mode, S0=S0.to(DEV))
+    torch.cuda.synchronize()
+    ro, rS = O.linattn_chunked_forward(f64(q), f64(k), f64(v), f64(eta), f64(S0), wl.chunk,
+                                       wl.mode)
+    assert max_rel(f64(o), ro) <= F32_MAX_REL
+    assert max_rel(f64(S), rS) <= F32_MAX_REL
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads
+
+def test_linattn_full_size():
+    """Linear-attention workload at full size (B4 H4 N8192 d128, chunk 2048)."""
+    cla = lib()
+    wl = W.LINATTN_C2
+    q, k, v, eta, _ = W.linattn_inputs(wl)
+    o, S = cla.linattn_chunked_forward(q.to(DEV), k.to(DEV), v.to(DEV), eta.to(DEV), wl.chunk,
+                                       wl.mode)
+    torch.cuda.synchronize()
+    assert_status_ok(cla)
+    ro, rS = O.linattn_chunked_forward(f64(q), f64(k), f64(v), f64(eta), None, wl.chunk, wl.mode)
+    assert rel_l2(f64(o), ro) <= BF16_REL_L2
+    assert rel_l2(f64(S), rS) <= BF16_REL_L2
+
+
+def test_layer_lm_full_size_sampled():
+    """LM-style workload at full size (B2 H4 d=m=384 N32768 chunk 2048, Muon 5,
+    beta 0.9): the outputs of the first two chunks against the oracle's
+    prefix scan, the weights after two chunks from a prefix call, and unit
+    row norms of the final weights."""
+    cla = lib()
+    wl = W.LM_760M
+    q, k, v, eta, W1, W2, W3 = W.layer_inputs(wl)
+    got = run_layer(cla, wl, q, k, v, eta, W1, W2, W3)
+    nc = 2
+    pre = wl.chunk * nc
+    ref = run_oracle(wl, q, k, v, eta, W1, W2, W3, n_chunks=nc)
+    assert rel_l2(got[0][..., :pre, :], ref[0][..., :pre, :]) <= BF16_MUON_REL_L2
+    for Wf in got[1:]:
+        np.testing.assert_allclose(np.linalg.norm(Wf, axis=-1), 1.0, atol=1e-3)
+    wp = dataclasses.replace(wl, N=pre)
+    sl = lambda t: t[..., :pre, :].contiguous()
+    gp = run_layer(cla, wp, sl(q), sl(k), sl(v), eta[..., :pre].contiguous(), W1, W2, W3)
+    errs = [rel_l2(g_, r_) for g_, r_ in zip(gp[1:], ref[1:4])]
+    assert max(errs) <= BF16_MUON_REL_L2, errs
+
+
+def test_layer_strided_full_size():
+    """View-synthesis strided workload at full size (B1 H2 d384 m768, 8 x 8192,
+    update on chunks 0-3): every output and final weight."""
+    cla = lib()
+    wl = W.NVS_STRIDED
+    inp = W.layer_inputs(wl)
+    got = run_layer(cla, wl, *inp)
+    ref = run_oracle(wl, *inp)
+    errs = [rel_l2(g_, r_) for g_, r_ in zip(got, ref[:4])]
+    assert max(errs) <= BF16_REL_L2, errs
