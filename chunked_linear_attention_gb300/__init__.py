@@ -31,8 +31,16 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libttt_gb300.so")
 EXPORTED = (
     "ttt_status_string", "ttt_layer_workspace_size", "ttt_layer_forward",
     "linattn_workspace_size", "linattn_chunked_forward", "ttt_device_status",
-    "ttt_set_wait_limit_ns", "ttt_selftest_gemm",
+    "ttt_set_wait_limit_ns", "ttt_selftest_gemm", "ttt_launch_count", "ttt_profile_start",
+    "ttt_profile_stop",
 )
+
+
+class ProfileEntry(ctypes.Structure):
+    """Mirror of ``ttt_profile_entry``."""
+    _fields_ = [("name", ctypes.c_char * 32), ("kernel", ctypes.c_char * 32),
+                ("launches", ctypes.c_int), ("ms", ctypes.c_double),
+                ("flops", ctypes.c_double), ("bytes", ctypes.c_double)]
 
 
 class UpdateRule(ctypes.Structure):
@@ -78,6 +86,12 @@ def _declare(lib):
     lib.ttt_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
     lib.ttt_selftest_gemm.restype = i
     lib.ttt_selftest_gemm.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, vp]
+    lib.ttt_launch_count.restype = ctypes.c_ulonglong
+    lib.ttt_launch_count.argtypes = []
+    lib.ttt_profile_start.restype = None
+    lib.ttt_profile_start.argtypes = []
+    lib.ttt_profile_stop.restype = i
+    lib.ttt_profile_stop.argtypes = [ctypes.POINTER(ProfileEntry), i]
     return lib
 
 
@@ -219,6 +233,25 @@ def linattn_chunked_forward(q, k, v, eta, chunk: int, mask_mode: int,
 def device_status(stream=None) -> int:
     """Synchronises the stream; returns and clears the device status word."""
     return library().ttt_device_status(_stream(stream))
+
+
+def launch_count() -> int:
+    """Kernels the library has launched in this process."""
+    return int(library().ttt_launch_count())
+
+
+def profile_start():
+    library().ttt_profile_start()
+
+
+def profile_stop():
+    """Per launch kind: dict(name, kernel, launches, ms, flops, bytes)."""
+    arr = (ProfileEntry * 32)()
+    n = library().ttt_profile_stop(arr, 32)
+    if n < 0:
+        raise TTTError(n, "ttt_profile_stop")
+    return [dict(name=e.name.decode(), kernel=e.kernel.decode(), launches=e.launches, ms=e.ms,
+                 flops=e.flops, bytes=e.bytes) for e in arr[:n]]
 
 
 def set_wait_limit_ns(ns: int):

@@ -4,6 +4,8 @@
 
 #include <cstring>
 
+#include "prof.h"
+
 namespace ttt {
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -127,9 +129,18 @@ bool LaunchBuilder::add(Problem p) {
   return true;
 }
 
-cudaError_t LaunchBuilder::launch(cudaStream_t stream) {
+cudaError_t LaunchBuilder::launch(cudaStream_t stream, int tag) {
   if (!ok_) return cudaErrorInvalidValue;
-  cudaError_t e = tc_ ? launch_umma_gemm(L_, stream) : launch_simt_gemm(L_, stream);
+  double flops = 0;
+  for (int i = 0; i < L_.nprob; ++i) {
+    const Problem& p = L_.prob[i];
+    flops += 2.0 * p.M * p.N * (double)p.K * p.Z * p.nacc;
+  }
+  cudaError_t e;
+  {
+    ProfScope ps(tag, stream, flops, 0.0);
+    e = tc_ ? launch_umma_gemm(L_, stream) : launch_simt_gemm(L_, stream);
+  }
   reset();
   return e;
 }

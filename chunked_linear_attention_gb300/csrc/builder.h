@@ -49,7 +49,8 @@ class LaunchBuilder {
   int choose_bn(int N, int nacc) const;
   // Fills tiles and appends.  Returns false when the launch is full.
   bool add(Problem p);
-  cudaError_t launch(cudaStream_t stream);
+  // Launches with launch accounting under profile tag `tag`.
+  cudaError_t launch(cudaStream_t stream, int tag);
   bool ok() const { return ok_; }
   bool tensor_cores() const { return tc_; }
   int bm() const { return tc_ ? 128 : kSimtTile; }

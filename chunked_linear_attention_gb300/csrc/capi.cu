@@ -3,8 +3,8 @@
 #include <cmath>
 #include <cstdint>
 
-#include "../../include/ttt.h"
-#include "../../include/ttt_selftest.h"
+#include "ttt.h"
+#include "ttt_selftest.h"
 #include "layer.h"
 
 namespace {

@@ -24,6 +24,7 @@
 
 #include "builder.h"
 #include "layer.h"
+#include "prof.h"
 
 namespace ttt {
 
@@ -132,6 +133,7 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
     ms[s].work = tc ? w.Wb[s] : nullptr;
     ms[s].rows = rows_of[s];
     ms[s].cols = cols_of[s];
+    ProfScope ps(PT_INIT, st, 0.0, (double)BH * rows_of[s] * cols_of[s] * (4 + 4 + (tc ? 2 : 0)));
     TTT_CK(launch_init_weights(ms[s], D.B, D.H, st));
   }
   float* mom[3];
@@ -141,8 +143,14 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
     else
       mom[s] = w.M ? w.M + (long long)s * BH * dm : nullptr;
   }
-  if (!a.momentum && w.M) TTT_CK(launch_copy_f32(w.M, nullptr, 3LL * BH * dm, st));
-  TTT_CK(launch_copy_f32(w.normsq, nullptr, 3LL * BH, st));
+  if (!a.momentum && w.M) {
+    ProfScope ps(PT_INIT, st, 0.0, 3.0 * BH * dm * 4);
+    TTT_CK(launch_copy_f32(w.M, nullptr, 3LL * BH * dm, st));
+  }
+  {
+    ProfScope ps(PT_INIT, st, 0.0, 3.0 * BH * 4);
+    TTT_CK(launch_copy_f32(w.normsq, nullptr, 3LL * BH, st));
+  }
   for (int s = 0; s < 3; ++s) {
     float* u_slot = w.U + (long long)s * BH * dm;
     ms[s].update = (!muon && mom[s]) ? mom[s] : u_slot;
@@ -228,7 +236,7 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
       LB.add(p);
     }
     if (!LB.ok()) return -4;
-    TTT_CK(LB.launch(st));
+    TTT_CK(LB.launch(st, PT_PROJ));
 
     // ---------------- GRAD (+ OUT)
     if (up >= 0) {
@@ -270,7 +278,7 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
       LB.add(p);
     }
     if (!LB.ok()) return -4;
-    TTT_CK(LB.launch(st));
+    TTT_CK(LB.launch(st, PT_GRAD));
 
     if (up < 0) continue;
 
@@ -314,7 +322,7 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
           LB.add(p);
         }
         if (!LB.ok()) return -4;
-        TTT_CK(LB.launch(st));
+        TTT_CK(LB.launch(st, PT_NS_GRAM));
         // POLY: Bm = b G + c G G (G symmetric)
         for (int g = 0; g < ng; ++g) {
           const int s0 = groups[g][0], cnt = groups[g][1];
@@ -335,7 +343,7 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
           LB.add(p);
         }
         if (!LB.ok()) return -4;
-        TTT_CK(LB.launch(st));
+        TTT_CK(LB.launch(st, PT_NS_POLY));
         // STEP: X' = s (a X + Bm X) (or X Bm for tall slots, in stored orientation)
         for (int g = 0; g < ng; ++g) {
           const int s0 = groups[g][0], cnt = groups[g][1];
@@ -369,13 +377,16 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
           LB.add(p);
         }
         if (!LB.ok()) return -4;
-        TTT_CK(LB.launch(st));
+        TTT_CK(LB.launch(st, PT_NS_STEP));
       }
     }
 
     // ---------------- NORM
-    TTT_CK(launch_update_normalize(ms, 3, BH, D.l2norm, muon ? w.normsq : nullptr,
-                                   muon ? 3 * BH : 0, st));
+    {
+      ProfScope ps(PT_NORM, st, 0.0, 3.0 * BH * dm * (4 + 4 + 4 + (tc ? 2 : 0)));
+      TTT_CK(launch_update_normalize(ms, 3, BH, D.l2norm, muon ? w.normsq : nullptr,
+                                     muon ? 3 * BH : 0, st));
+    }
   }
 #undef TTT_CK
   return 0;

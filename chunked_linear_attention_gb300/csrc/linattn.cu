@@ -16,6 +16,7 @@
 #include "builder.h"
 #include "layer.h"
 #include "linattn_kernels.h"
+#include "prof.h"
 
 namespace ttt {
 
@@ -100,8 +101,12 @@ int linattn_forward(const LinArgs& a, const LinDims& D, int* status, unsigned lo
     for (int c = 0; c < nc; ++c)
       if (a.update_chunks[c]) flags.bits[c >> 5] |= 1u << (c & 31);
 
-  if (launch_scale_rows(a.v, a.eta, w.Vt, (long long)BH * N, dv, tc, st) != cudaSuccess)
-    return -6;
+  {
+    const size_t es = tc ? 2 : 4;
+    ProfScope ps(PT_LIN_SCALE, st, 0.0, (double)BH * N * (dv * es * 2 + 4));
+    if (launch_scale_rows(a.v, a.eta, w.Vt, (long long)BH * N, dv, tc, st) != cudaSuccess)
+      return -6;
+  }
 
   MapCache cache;
   LaunchBuilder LB(tc, &cache, status, wait_ns);
@@ -122,11 +127,15 @@ int linattn_forward(const LinArgs& a, const LinDims& D, int* status, unsigned lo
     p.epi.out_z = (long long)dv * dk;
     LB.add(p);
     if (!LB.ok()) return -4;
-    if (LB.launch(st) != cudaSuccess) return -6;
+    if (LB.launch(st, PT_LIN_PARTIAL) != cudaSuccess) return -6;
   }
-  if (launch_linattn_prefix(w.partials, a.S0, w.Sread, a.S_final, BH, nc, splits, dv * dk,
-                            D.mode == 0, flags, tc, st) != cudaSuccess)
-    return -6;
+  {
+    ProfScope ps(PT_LIN_PREFIX, st, 0.0,
+                 (double)BH * nc * dv * dk * (4.0 * splits + (tc ? 2 : 4)));
+    if (launch_linattn_prefix(w.partials, a.S0, w.Sread, a.S_final, BH, nc, splits, dv * dk,
+                              D.mode == 0, flags, tc, st) != cudaSuccess)
+      return -6;
+  }
   {  // outputs
     const int bn = LB.choose_bn(dv, 1);
     Problem p = prob0(b, dv, dk, BH * nc, 1, bn);
@@ -138,7 +147,7 @@ int linattn_forward(const LinArgs& a, const LinDims& D, int* status, unsigned lo
     p.epi.out_z = (long long)b * dv;
     LB.add(p);
     if (!LB.ok()) return -4;
-    if (LB.launch(st) != cudaSuccess) return -6;
+    if (LB.launch(st, PT_LIN_OUT) != cudaSuccess) return -6;
   }
   return 0;
 }
@@ -162,7 +171,7 @@ int selftest_gemm(const void* A, const void* Bp, float* Dp, int Z, int M, int N,
   p.epi.out_z = (long long)M * N;
   LB.add(p);
   if (!LB.ok()) return -4;
-  return LB.launch(stream) == cudaSuccess ? 0 : -6;
+  return LB.launch(stream, PT_SELFTEST) == cudaSuccess ? 0 : -6;
 }
 
 }  // namespace ttt

@@ -1,0 +1,37 @@
+// Launch accounting: a process-wide launch counter and, while a profile
+// records, CUDA events around each launch with its algorithmic work.
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace ttt {
+
+enum ProfTag : int {
+  PT_INIT = 0,
+  PT_PROJ,
+  PT_GRAD,
+  PT_NS_GRAM,
+  PT_NS_POLY,
+  PT_NS_STEP,
+  PT_NORM,
+  PT_LIN_SCALE,
+  PT_LIN_PARTIAL,
+  PT_LIN_PREFIX,
+  PT_LIN_OUT,
+  PT_SELFTEST,
+  PT_COUNT
+};
+
+// Records (when profiling) an event before the launch; the destructor
+// records the one after and counts the launch.
+class ProfScope {
+ public:
+  ProfScope(int tag, cudaStream_t s, double flops, double bytes);
+  ~ProfScope();
+
+ private:
+  int idx_;
+  cudaStream_t s_;
+};
+
+}  // namespace ttt

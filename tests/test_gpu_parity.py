@@ -129,8 +129,9 @@ BF16_CASES = [
 @pytest.mark.parametrize("case", BF16_CASES)
 def test_layer_bf16_variants(case):
     cla = lib()
-    wl = dataclasses.replace(W.LM_760M, B=2, H=2, muon_steps=0, momentum_beta=0.0,
-                             l2_normed_k=False, **case)
+    base = dict(B=2, H=2, muon_steps=0, momentum_beta=0.0, l2_normed_k=False)
+    base.update(case)
+    wl = dataclasses.replace(W.LM_760M, **base)
     inp = W.layer_inputs(wl)
     got = run_layer(cla, wl, *inp)
     ref = run_oracle(wl, *inp)
