@@ -32,7 +32,7 @@ EXPORTED = (
     "ttt_status_string", "ttt_layer_workspace_size", "ttt_layer_forward",
     "linattn_workspace_size", "linattn_chunked_forward", "ttt_device_status",
     "ttt_set_wait_limit_ns", "ttt_selftest_gemm", "ttt_launch_count", "ttt_profile_start",
-    "ttt_profile_stop",
+    "ttt_profile_stop", "linattn_chunked_forward_noalloc",
 )
 
 
@@ -86,6 +86,9 @@ def _declare(lib):
     lib.ttt_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
     lib.ttt_selftest_gemm.restype = i
     lib.ttt_selftest_gemm.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, vp]
+    lib.linattn_chunked_forward_noalloc.restype = i
+    lib.linattn_chunked_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i,
+                                                    vp, vp, vp, vp]
     lib.ttt_launch_count.restype = ctypes.c_ulonglong
     lib.ttt_launch_count.argtypes = []
     lib.ttt_profile_start.restype = None
@@ -227,6 +230,32 @@ def linattn_chunked_forward(q, k, v, eta, chunk: int, mask_mode: int,
                                      _stream(stream))
     del keep
     _check(rc, "linattn_chunked_forward")
+    return out, S_final
+
+
+def linattn_chunked_forward_noalloc(q, k, v, eta, chunk: int, mask_mode: int,
+                                    S0: Optional[torch.Tensor] = None,
+                                    update_chunks: Optional[Sequence[int]] = None,
+                                    out: Optional[torch.Tensor] = None,
+                                    S_final: Optional[torch.Tensor] = None, stream=None):
+    """Chunked linear attention whose scratch is the library's fixed 16 MiB
+    device array instead of a workspace (see
+    ``linattn_chunked_forward_noalloc`` in include/ttt.h).  Output tensors are
+    still the caller's (allocated here with torch when not given)."""
+    lib = library()
+    B, H, N, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, H, N, dv), device=dev, dtype=q.dtype)
+    if S_final is None:
+        S_final = torch.empty((B, H, dv, dk), device=dev, dtype=torch.float32)
+    keep, fl = _flags(update_chunks, N // chunk if chunk > 0 else 0)
+    rc = lib.linattn_chunked_forward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(eta), _ptr(S0), B, H,
+                                             N, dk, dv, chunk, _io_dtype(q), mask_mode, fl,
+                                             _ptr(out), _ptr(S_final), _stream(stream))
+    del keep
+    _check(rc, "linattn_chunked_forward_noalloc")
     return out, S_final
 
 

@@ -162,6 +162,28 @@ int linattn_chunked_forward(const void* q, const void* k, const void* v, const f
                             void* out, float* S_final,
                             void* workspace, size_t workspace_bytes, ttt_stream_t stream);
 
+/* linattn_chunked_forward for callers that cannot allocate device memory.
+ * The pages have no counterpart for this call; it exists because some
+ * callers cannot call cudaMalloc (a host framework that owns the GPU memory
+ * pool and forbids outside allocations, or a latency-critical loop that
+ * cannot afford cudaMalloc's implicit device synchronisation), so they cannot
+ * provide the workspace the regular call needs.
+ *
+ * Same arguments and results as linattn_chunked_forward, without the
+ * workspace: the scratch comes from a fixed 16 MiB array in device memory
+ * that every GPU loading the library reserves until the process exits.
+ * Allocates nothing.  Problems whose linattn_workspace_size() exceeds 16 MiB
+ * return TTT_ERR_WORKSPACE before anything is enqueued.  The first call on
+ * each device looks up the array's device address with a runtime call (with
+ * that device current), so make it before any stream capture begins.  All
+ * calls share the array: calls that overlap on the GPU (e.g. concurrently on
+ * two streams) race on it and must be serialised by the caller. */
+int linattn_chunked_forward_noalloc(const void* q, const void* k, const void* v,
+                                    const float* eta, const float* S0, int B, int H, int N,
+                                    int d_k, int d_v, int chunk, int io_dtype, int mask_mode,
+                                    const unsigned char* update_chunks, void* out,
+                                    float* S_final, ttt_stream_t stream);
+
 /* Synchronises `stream`, then returns and clears the device status word:
  * TTT_OK, TTT_ERR_TIMEOUT if a kernel's bounded wait ran out since the last
  * call, or TTT_ERR_CUDA if the synchronisation itself failed. */
