@@ -101,7 +101,8 @@ OpDesc LaunchBuilder::op(const TensorRef& t, int mn_major, int outer_base, int z
 
 int LaunchBuilder::choose_bn(int N, int nacc) const {
   if (!tc_) return kSimtTile;
-  int max_bn = nacc >= 3 ? 128 : 256;
+  // nacc >= 2: bn <= 128 so that accumulators sharing A merge into one N <= 256 MMA
+  int max_bn = nacc >= 2 ? 128 : 256;
   int best = 64;
   long long best_area = -1;
   for (int bn = max_bn; bn >= 64; bn -= 64) {

@@ -14,64 +14,74 @@
 //   EPI_NS_GRAM  A = s^2 X X^T,     s = 1/(|M|_F + eps) on the first step
 //   EPI_NS_POLY  B = b A + c A A
 //   EPI_NS_STEP  X' = s (a X + B X)  (work type, or fp32 U on the last step)
+//
+// All packing is done in registers (no address-taken local arrays), so the
+// epilogue never touches local memory.
 #pragma once
 
 #include "common.cuh"
 
 namespace ttt {
 
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+// Stores V values; vector path when all V are valid and dst is 16-byte aligned.
 template <typename T, int V>
-__device__ __forceinline__ void store_vec(T* dst, const float* v, int n) {
+__device__ __forceinline__ void store_vec(T* dst, const float (&v)[V], int n) {
   if constexpr (sizeof(T) == 2) {
-    if (n == V && V % 8 == 0 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+    if (V % 8 == 0 && n == V && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
 #pragma unroll
-      for (int i = 0; i < V; i += 8) {
-        __nv_bfloat162 p[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) p[k] = __floats2bfloat162_rn(v[i + 2 * k], v[i + 2 * k + 1]);
-        *reinterpret_cast<uint4*>(dst + i) = *reinterpret_cast<uint4*>(p);
-      }
+      for (int i = 0; i < V; i += 8)
+        *reinterpret_cast<uint4*>(dst + i) =
+            make_uint4(pack_bf16x2(v[i], v[i + 1]), pack_bf16x2(v[i + 2], v[i + 3]),
+                       pack_bf16x2(v[i + 4], v[i + 5]), pack_bf16x2(v[i + 6], v[i + 7]));
       return;
     }
   } else {
-    if (n == V && V % 4 == 0 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+    if (V % 4 == 0 && n == V && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
 #pragma unroll
       for (int i = 0; i < V; i += 4)
         *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
       return;
     }
   }
-  for (int i = 0; i < n; ++i) dst[i] = from_f<T>(v[i]);
+#pragma unroll
+  for (int i = 0; i < V; ++i)
+    if (i < n) dst[i] = from_f<T>(v[i]);
 }
 
 template <typename T, int V>
-__device__ __forceinline__ void load_vec(const T* src, float* v, int n) {
+__device__ __forceinline__ void load_vec(const T* src, float (&v)[V], int n) {
   if constexpr (sizeof(T) == 2) {
-    if (n == V && V % 8 == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+    if (V % 8 == 0 && n == V && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
 #pragma unroll
       for (int i = 0; i < V; i += 8) {
-        uint4 raw = *reinterpret_cast<const uint4*>(src + i);
-        const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float2 f = __bfloat1622float2(p[k]);
-          v[i + 2 * k] = f.x;
-          v[i + 2 * k + 1] = f.y;
-        }
+        const uint4 r = *reinterpret_cast<const uint4*>(src + i);
+        v[i] = bf16lo(r.x); v[i + 1] = bf16hi(r.x);
+        v[i + 2] = bf16lo(r.y); v[i + 3] = bf16hi(r.y);
+        v[i + 4] = bf16lo(r.z); v[i + 5] = bf16hi(r.z);
+        v[i + 6] = bf16lo(r.w); v[i + 7] = bf16hi(r.w);
       }
       return;
     }
   } else {
-    if (n == V && V % 4 == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+    if (V % 4 == 0 && n == V && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
 #pragma unroll
       for (int i = 0; i < V; i += 4) {
-        float4 f = *reinterpret_cast<const float4*>(src + i);
+        const float4 f = *reinterpret_cast<const float4*>(src + i);
         v[i] = f.x; v[i + 1] = f.y; v[i + 2] = f.z; v[i + 3] = f.w;
       }
       return;
     }
   }
-  for (int i = 0; i < n; ++i) v[i] = to_f<T>(src[i]);
+#pragma unroll
+  for (int i = 0; i < V; ++i) v[i] = i < n ? to_f<T>(src[i]) : 0.f;
 }
 
 // 1 / (|M|_F + eps) from an accumulated squared norm.
@@ -85,8 +95,8 @@ __device__ __forceinline__ float ns_scale(const EpiDesc& e, int z) {
 // of the values EPI_GRAD routes to the Newton-Schulz input (else 0).
 template <int V, typename WT, typename IOT, bool kPrecise>
 __device__ __forceinline__ float epilogue_vec(const EpiDesc& e, int z, int r, int c, int n,
-                                              const float* a0, const float* a1,
-                                              const float* a2) {
+                                              const float (&a0)[V], const float (&a1)[V],
+                                              const float (&a2)[V]) {
   const int zz = e.z_div > 1 ? z / e.z_div : z;
   const long long idx = (long long)zz * e.out_z + (e.out_row0 + r) * e.out_ld + c;
   float o[V];
@@ -149,8 +159,9 @@ __device__ __forceinline__ float epilogue_vec(const EpiDesc& e, int z, int r, in
     }
     case EPI_NS_GRAM: {
       const float s = e.first ? ns_scale(e, zz) : 1.0f;
+      const float s2 = s * s;
 #pragma unroll
-      for (int i = 0; i < V; ++i) o[i] = a0[i] * s * s;
+      for (int i = 0; i < V; ++i) o[i] = a0[i] * s2;
       store_vec<WT, V>(static_cast<WT*>(e.out[0]) + idx, o, n);
       break;
     }

@@ -1,221 +1,176 @@
-// Grouped batched GEMM on the 5th-generation tensor cores (tcgen05 + TMEM),
-// operands staged by TMA into 128-byte-swizzled shared memory, with the fused
-// epilogues of epilogue.cuh.  One CTA computes one 128 x bn output tile of one
-// batch index of one problem, holding up to three fp32 accumulators in TMEM.
+// Persistent grouped batched GEMM on the 5th-generation tensor cores (tcgen05
+// + TMEM), operands staged by TMA into 128-byte-swizzled shared memory, fused
+// epilogues from epilogue.cuh.
 //
-// Warp roles (192 threads): warp 0 issues TMA loads into a ring of stages,
-// warp 1 owns the TMEM allocation and issues tcgen05.mma from one thread,
-// warps 2..5 drain TMEM (tcgen05.ld) and run the epilogue, warp w reading
-// TMEM lanes 32*(w%4)..+31 (one output row per thread).  Every wait is bounded
+// One CTA per SM (the whole 227 KB of shared memory, all 512 TMEM columns)
+// walks the launch's tiles with a static stride of gridDim.x.  Warp roles
+// (192 threads): warp 0 issues TMA loads into a ring of stages, warp 1 issues
+// tcgen05.mma from one thread, warps 2..5 drain TMEM (tcgen05.ld) and run the
+// epilogue.  When a tile needs at most 256 TMEM columns the accumulator is
+// double-buffered, so the epilogue of one tile overlaps the MMAs of the next;
+// the producer always runs ahead into the next tile.  Every wait is bounded
 // and reports TTT_ERR_TIMEOUT into the device status word.
-#include "common.cuh"
-#include "epilogue.cuh"
 #include "launch.h"
+#include "tc_epilogue.cuh"
+#include "umma_core.cuh"
 
 namespace ttt {
 
 static_assert(sizeof(GemmLaunch) <= 4096, "kernel parameter block too large");
 
-constexpr int kUmmaThreads = 192;
-constexpr int kBM = 128;
-constexpr int kBK = 64;                      // one 128-byte swizzle row of bf16
-constexpr int kATileBytes = kBM * kBK * 2;   // 16 KB
-constexpr int kMaxStages = 8;
-constexpr int kCtrlBytes = 1024;             // barriers + TMEM slot
-
-struct TileCoord {
-  int prob, z, tm, tn;
-};
-
-__device__ __forceinline__ TileCoord decode_tile(const GemmLaunch& L, int t) {
-  int p = 0;
-#pragma unroll 1
-  for (int i = 1; i < L.nprob; ++i)
-    if (t >= L.prob[i].tile_start) p = i;
-  const Problem& P = L.prob[p];
-  int local = t - P.tile_start;
-  TileCoord c;
-  c.prob = p;
-  c.tn = local % P.tiles_n;
-  local /= P.tiles_n;
-  c.tm = local % P.tiles_m;
-  c.z = local / P.tiles_m;
-  return c;
-}
-
-// Issue the TMA boxes of one operand tile (rows x 64 of K) for k-step ks.
-__device__ __forceinline__ void load_operand(const GemmLaunch& L, const OpDesc& op, uint8_t* dst,
-                                             int rows, int mn0, int ks, int z, uint64_t* bar) {
-  const int zz = op.z_div > 1 ? z / op.z_div : z;
-  const CUtensorMap* map = &L.maps[op.map];
-  if (!op.mn_major) {
-    tma_load_2d(dst, map, op.inner_base + ks * kBK, op.outer_base + zz * op.z_outer + mn0, bar);
-  } else {
-    for (int i = 0; i < rows / 64; ++i)
-      tma_load_2d(dst + i * 8192, map, op.inner_base + mn0 + i * 64,
-                  op.outer_base + zz * op.z_outer + ks * kBK, bar);
-  }
-}
-
-__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int mn_major, int kk) {
-  // K-major: a 16-element K slice starts 32 bytes further along the row.
-  // MN-major: it starts 16 K-rows (2 KB) further down.
-  return mn_major ? smem_desc_sw128(base + kk * 2048, 8192, 1024)
-                  : smem_desc_sw128(base + kk * 32, 16, 1024);
-}
-
-__global__ void __launch_bounds__(kUmmaThreads, 1)
+__global__ void __launch_bounds__(kGemmThreads, 1)
     umma_gemm_kernel(const __grid_constant__ GemmLaunch L) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
-  uint64_t* accf = empty + kMaxStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
-  uint8_t* tiles = smem + kCtrlBytes;
+  uint64_t* accf = empty + kMaxStages;   // [2] accumulator ready (MMA -> epilogue)
+  uint64_t* acce = accf + 2;             // [2] accumulator free (epilogue -> MMA)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
+  float* staging = reinterpret_cast<float*>(smem + kCtrlBytes);
+  uint8_t* tiles = smem + kCtrlBytes + kStagingBytes;
+  // The problem descriptors are read in every loop of every role: keep a copy
+  // in shared memory (parameter space behind a generic pointer is slow).
+  Problem* probs = reinterpret_cast<Problem*>(smem + kProbOffset);
+  static_assert(kProbOffset + kMaxProblems * sizeof(Problem) <= kCtrlBytes, "control region");
 
-  const TileCoord tc = decode_tile(L, blockIdx.x);
-  const Problem& P = L.prob[tc.prob];
-  const int nacc = P.nacc, bn = P.bn;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  {
+    const uint32_t* sw = reinterpret_cast<const uint32_t*>(L.prob);
+    uint32_t* dw = reinterpret_cast<uint32_t*>(probs);
+    const int words = (int)(L.nprob * sizeof(Problem) / 4);
+    for (int i = threadIdx.x; i < words; i += blockDim.x) dw[i] = sw[i];
+  }
+  const int nprob = L.nprob, total_tiles = L.total_tiles;
+  __syncthreads();
 
-  uint32_t a_off[kMaxAcc], b_off[kMaxAcc], stage_bytes = 0, tx_bytes = 0;
-#pragma unroll
-  for (int j = 0; j < kMaxAcc; ++j) {
-    if (j >= nacc) break;
-    if (j > 0 && ((P.a_shared >> j) & 1)) {
-      a_off[j] = a_off[j - 1];
-    } else {
-      a_off[j] = stage_bytes;
-      stage_bytes += kATileBytes;
-    }
+  // one stage layout for the whole launch: the largest problem's
+  uint32_t stage_bytes = 0;
+  int max_cols = 0;
+  for (int p = 0; p < nprob; ++p) {
+    SmemPlan sp;
+    plan_problem(probs[p], sp);
+    stage_bytes = max(stage_bytes, sp.max_bytes);
+    max_cols = max(max_cols, probs[p].nacc * probs[p].bn);
   }
-#pragma unroll
-  for (int j = 0; j < kMaxAcc; ++j) {
-    if (j >= nacc) break;
-    b_off[j] = stage_bytes;
-    stage_bytes += bn * kBK * 2;
-  }
-  tx_bytes = stage_bytes;
-  int nstages = (kUmmaSmemBytes - 1024 - kCtrlBytes) / (int)stage_bytes;
+  int nstages = (kUmmaSmemBytes - 1024 - kCtrlBytes - kStagingBytes) / (int)stage_bytes;
   if (nstages > kMaxStages) nstages = kMaxStages;
-  const int nk = P.K / kBK;
-  uint32_t ncols = 32;
-  while (ncols < (uint32_t)(nacc * bn)) ncols <<= 1;
+  const int nbuf = max_cols <= 256 ? 2 : 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < nstages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(accf, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf[b], 1);
+      mbar_init(&acce[b], kEpiWarps);
+    }
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    for (int j = 0; j < nacc; ++j) {
-      tma_prefetch_map(&L.maps[P.a[j].map]);
-      tma_prefetch_map(&L.maps[P.b[j].map]);
-    }
+    for (int p = 0; p < nprob; ++p)
+      for (int j = 0; j < probs[p].nacc; ++j) {
+        tma_prefetch_map(&L.maps[probs[p].a[j].map]);
+        tma_prefetch_map(&L.maps[probs[p].b[j].map]);
+      }
   }
-  if (warp == 1) tmem_alloc(tmem_slot, ncols);
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const unsigned long long lim = L.wait_limit_ns;
 
-  if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer
-    int issued = 0;
-    for (int ks = 0; ks < nk; ++ks) {
-      const int s = ks % nstages;
-      const uint32_t ph = (ks / nstages) & 1;
-      if (!mbar_wait(&empty[s], ph ^ 1, L.status, lim)) break;
-      mbar_arrive_expect_tx(&full[s], tx_bytes);
-      uint8_t* st = tiles + s * stage_bytes;
-      for (int j = 0; j < nacc; ++j) {
-        if (!(j > 0 && ((P.a_shared >> j) & 1)))
-          load_operand(L, P.a[j], st + a_off[j], kBM, tc.tm * kBM, ks, tc.z, &full[s]);
-        load_operand(L, P.b[j], st + b_off[j], bn, tc.tn * bn, ks, tc.z, &full[s]);
+  if (warp == 0) {
+    if (lane == 0) {
+      int s = 0, filled = 0;
+      uint32_t ph = 0;
+      for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+        const TileCoord tc = decode_tile(probs, nprob, t);
+        const Problem& P = probs[tc.prob];
+        SmemPlan sp;
+        plan_problem(P, sp);
+        filled += sp.ngroups * (P.K / kBK);
+        if (!produce_tile(L.maps, P, sp, tc, tiles, stage_bytes, nstages, full, empty, s, ph,
+                          L.status, lim))
+          break;
       }
-      issued = ks + 1;
+      drain_producer(full, nstages, s, ph, filled, L.status, lim);
     }
-    // wait (bounded) until the copies of the last stages have landed
-    for (int ks = issued > nstages ? issued - nstages : 0; ks < issued; ++ks)
-      mbar_wait(&full[ks % nstages], (ks / nstages) & 1, L.status, lim);
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer
-    uint32_t idesc[kMaxAcc];
-    for (int j = 0; j < nacc; ++j) idesc[j] = idesc_bf16_f32(bn, P.a[j].mn_major, P.b[j].mn_major);
-    for (int ks = 0; ks < nk; ++ks) {
-      const int s = ks % nstages;
-      const uint32_t ph = (ks / nstages) & 1;
-      if (!mbar_wait(&full[s], ph, L.status, lim)) break;
-      tc_fence_after();
-      const uint32_t st = smem_u32(tiles + s * stage_bytes);
-      for (int j = 0; j < nacc; ++j) {
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int s = 0, it = 0;
+      uint32_t ph = 0;
+      const uint32_t tiles_saddr = smem_u32(tiles);
+      for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
+        const TileCoord tc = decode_tile(probs, nprob, t);
+        const Problem& P = probs[tc.prob];
+        SmemPlan sp;
+        plan_problem(P, sp);
+        const int buf = it % nbuf;
+        const uint32_t bph = (it / nbuf) & 1;
+        if (!mbar_wait(&acce[buf], bph ^ 1, L.status, lim)) break;
+        tc_fence_after();
+        const bool ok = mma_tile(P, sp, tiles_saddr, stage_bytes, nstages, full, empty,
+                                 tmem + buf * 256, s, ph, L.status, lim);
+        umma_commit(&accf[buf]);
+        if (!ok) break;
+      }
+    }
+  } else {
+    int it = 0;
+    float* stage = staging + (warp - 2) * kStageFloats;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
+      const TileCoord tc = decode_tile(probs, nprob, t);
+      const Problem& P = probs[tc.prob];
+      const int buf = it % nbuf;
+      const uint32_t bph = (it / nbuf) & 1;
+      bool ok = false;
+      const float sumsq = tc_epilogue_tile(P, tc.z, tc.tm, tc.tn, tmem + buf * 256, &accf[buf], bph,
+                                           L.status, lim, &ok, stage, warp, lane);
+      if (P.epi.kind == EPI_GRAD && P.epi.normsq_out) {
+        float ss = sumsq;
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          const uint64_t ad = operand_desc(st + a_off[j], P.a[j].mn_major, kk);
-          const uint64_t bd = operand_desc(st + b_off[j], P.b[j].mn_major, kk);
-          umma_bf16(tmem + j * bn, ad, bd, idesc[j], (ks | kk) != 0);
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        if (lane == 0) {
+          const int zz = P.epi.z_div > 1 ? tc.z / P.epi.z_div : tc.z;
+          atomicAdd(P.epi.normsq_out + zz, ss);
         }
       }
-      umma_commit(&empty[s]);
-    }
-    umma_commit(accf);
-  } else if (warp >= 2) {
-    // ---------------- epilogue
-    const bool ok = mbar_wait(accf, 0, L.status, lim);
-    tc_fence_after();
-    const int sub = warp & 3;
-    const int row = sub * 32 + lane;
-    const int grow = tc.tm * kBM + row;
-    const uint32_t tl = tmem + ((uint32_t)(sub * 32) << 16);
-    float sumsq = 0.f;
-    if (ok) {
-      for (int c0 = 0; c0 < bn; c0 += 16) {
-        float v0[16], v1[16], v2[16];
-        tmem_ld16(tl + c0, v0);
-        if (nacc > 1) tmem_ld16(tl + bn + c0, v1);
-        if (nacc > 2) tmem_ld16(tl + 2 * bn + c0, v2);
-        const int gcol = tc.tn * bn + c0;
-        if (grow < P.M && gcol < P.N) {
-          const int n = min(16, P.N - gcol);
-          sumsq += epilogue_vec<16, __nv_bfloat16, __nv_bfloat16, false>(P.epi, tc.z, grow, gcol,
-                                                                        n, v0, v1, v2);
-        }
-      }
-    }
-    if (P.epi.kind == EPI_GRAD && P.epi.normsq_out) {
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sumsq += __shfl_xor_sync(0xffffffffu, sumsq, off);
-      if (lane == 0) {
-        const int zz = P.epi.z_div > 1 ? tc.z / P.epi.z_div : tc.z;
-        atomicAdd(P.epi.normsq_out + zz, sumsq);
-      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce[buf]);
+      if (!ok) break;
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, ncols);
+    tmem_dealloc(tmem, 512);
   }
 }
 
 cudaError_t launch_umma_gemm(const GemmLaunch& L, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(umma_gemm_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kUmmaSmemBytes);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static int attr_done[64] = {0};
+  static int sm_count[64] = {0};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dev]) {
+    e = cudaFuncSetAttribute(umma_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kUmmaSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = 1;
   }
   if (L.total_tiles <= 0) return cudaSuccess;
-  umma_gemm_kernel<<<L.total_tiles, kUmmaThreads, kUmmaSmemBytes, stream>>>(L);
+  const int grid = L.total_tiles < sm_count[dev] ? L.total_tiles : sm_count[dev];
+  umma_gemm_kernel<<<grid, kGemmThreads, kUmmaSmemBytes, stream>>>(L);
   return cudaGetLastError();
 }
 

@@ -24,6 +24,7 @@
 
 #include "builder.h"
 #include "layer.h"
+#include "ns_cluster.h"
 #include "prof.h"
 
 namespace ttt {
@@ -283,7 +284,31 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
     if (up < 0) continue;
 
     // ---------------- MUON (Newton-Schulz on M, every matrix)
-    if (muon) {
+    bool fused_update = false;
+    if (muon && tc && d == m) {
+      NsArgs na;
+      na.X[0] = w.X[0];
+      na.X[1] = w.X[1];
+      na.G = w.G;
+      na.Bm = w.Bm;
+      na.U = w.U;
+      na.normsq = w.normsq;
+      for (int s = 0; s < 3; ++s) {
+        na.W[s] = ms[s].master;
+        na.Wb[s] = ms[s].work;
+      }
+      na.BH = BH;
+      na.d = d;
+      na.steps = D.muon_steps;
+      na.l2norm = D.l2norm;
+      na.ns[0] = D.ns[0];
+      na.ns[1] = D.ns[1];
+      na.ns[2] = D.ns[2];
+      const int rc = launch_ns_cluster(cache, na, status, wait_ns, st);
+      if (rc < 0) return rc;
+      fused_update = rc == 0;
+    }
+    if (muon && !fused_update) {
       const int sdim = std::min(d, m);
       // groups of equally shaped slots: {0,1,2} if square, else {0,1} and {2}
       int groups[2][2];  // first slot, count
@@ -382,7 +407,7 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
     }
 
     // ---------------- NORM
-    {
+    if (!fused_update) {
       ProfScope ps(PT_NORM, st, 0.0, 3.0 * BH * dm * (4 + 4 + 4 + (tc ? 2 : 0)));
       TTT_CK(launch_update_normalize(ms, 3, BH, D.l2norm, muon ? w.normsq : nullptr,
                                      muon ? 3 * BH : 0, st));

@@ -19,6 +19,7 @@ enum ProfTag : int {
   PT_LIN_PREFIX,
   PT_LIN_OUT,
   PT_SELFTEST,
+  PT_MUON,
   PT_COUNT
 };
 

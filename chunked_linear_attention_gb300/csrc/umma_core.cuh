@@ -1,0 +1,233 @@
+// Building blocks of the tensor-core kernels: tile decoding, the shared-memory
+// stage plan of a problem, and the three warp roles (TMA producer, tcgen05
+// MMA issuer, TMEM epilogue) for one 128 x bn output tile.  The persistent
+// grouped GEMM (gemm_umma.cu) and the cluster Newton-Schulz kernel
+// (ns_cluster.cu) run these roles over their own tile sequences; the
+// pipeline counters (k-step and tile iteration) carry across tiles so the
+// mbarrier phases stay consistent.
+#pragma once
+
+#include "common.cuh"
+#include "epilogue.cuh"
+
+namespace ttt {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;                      // one 128-byte swizzle row of bf16
+constexpr int kATileBytes = kBM * kBK * 2;   // 16 KB
+constexpr int kMaxStages = 8;
+constexpr int kCtrlBytes = 3072;             // barriers, TMEM slot, problem descriptors
+constexpr int kProbOffset = 256;             // problem descriptors inside the control region
+constexpr int kEpiWarps = 4;            // one warp per TMEM lane quarter
+constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
+
+struct TileCoord {
+  int prob, z, tm, tn;
+};
+
+__device__ __forceinline__ TileCoord decode_tile(const Problem* probs, int nprob, int t) {
+  int p = 0;
+#pragma unroll 1
+  for (int i = 1; i < nprob; ++i)
+    if (t >= probs[i].tile_start) p = i;
+  const Problem& P = probs[p];
+  int local = t - P.tile_start;
+  TileCoord c;
+  c.prob = p;
+  c.tn = local % P.tiles_n;
+  local /= P.tiles_n;
+  c.tm = local % P.tiles_m;
+  c.z = local / P.tiles_m;
+  return c;
+}
+
+// Accumulator groups of a problem.  Accumulators that share one A tile form a
+// group; a group's k-steps stream A plus the group's B tiles through one
+// pipeline stage (A at offset 0, B tiles after it), and the groups run one
+// after the other, so a stage never holds more than one A tile.  A group
+// whose B tiles are of the same major-ness and total N <= 256 is issued as a
+// single MMA (TMEM columns of its accumulators are adjacent).
+struct SmemPlan {
+  int ngroups;
+  int g_first[kMaxAcc], g_count[kMaxAcc], g_merged[kMaxAcc];
+  uint32_t g_bytes[kMaxAcc];
+  uint32_t max_bytes;
+};
+
+__device__ __forceinline__ void plan_problem(const Problem& P, SmemPlan& sp) {
+  sp.ngroups = 0;
+  sp.max_bytes = 0;
+  int j = 0;
+#pragma unroll 1
+  while (j < P.nacc) {
+    int cnt = 1;
+    while (j + cnt < P.nacc && ((P.a_shared >> (j + cnt)) & 1)) ++cnt;
+    bool same = true;
+    for (int i = 1; i < cnt; ++i) same = same && P.b[j + i].mn_major == P.b[j].mn_major;
+    const int g = sp.ngroups++;
+    sp.g_first[g] = j;
+    sp.g_count[g] = cnt;
+    sp.g_merged[g] = cnt > 1 && same && cnt * P.bn <= 256;
+    sp.g_bytes[g] = kATileBytes + cnt * P.bn * kBK * 2;
+    sp.max_bytes = max(sp.max_bytes, sp.g_bytes[g]);
+    j += cnt;
+  }
+}
+
+// Issue the TMA boxes of one operand tile (rows x 64 of K) for k-step ks.
+__device__ __forceinline__ void load_operand(const CUtensorMap* maps, const OpDesc& op,
+                                             uint8_t* dst, int rows, int mn0, int ks, int z,
+                                             uint64_t* bar) {
+  const int zz = op.z_div > 1 ? z / op.z_div : z;
+  const CUtensorMap* map = &maps[op.map];
+  if (!op.mn_major) {
+    tma_load_2d(dst, map, op.inner_base + ks * kBK, op.outer_base + zz * op.z_outer + mn0, bar);
+  } else {
+    for (int i = 0; i < rows / 64; ++i)
+      tma_load_2d(dst + i * 8192, map, op.inner_base + mn0 + i * 64,
+                  op.outer_base + zz * op.z_outer + ks * kBK, bar);
+  }
+}
+
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int mn_major, int kk) {
+  // K-major: a 16-element K slice starts 32 bytes further along the row.
+  // MN-major: it starts 16 K-rows (2 KB) further down.
+  return mn_major ? smem_desc_sw128(base + kk * 2048, 8192, 1024)
+                  : smem_desc_sw128(base + kk * 32, 16, 1024);
+}
+
+// ---------------------------------------------------------------- roles
+
+// Precomputed TMA coordinates of one operand tile: the k-step ks box(es) are
+// at (x0 + ks * dx, y0 + ks * dy) and, for MN-major operands, nbox boxes of 64
+// M/N columns 64 apart along x.
+struct OpCoords {
+  const CUtensorMap* map;
+  int x0, y0, dx, dy, nbox;
+};
+
+__device__ __forceinline__ OpCoords op_coords(const CUtensorMap* maps, const OpDesc& op, int rows,
+                                              int mn0, int z) {
+  const int zz = op.z_div > 1 ? z / op.z_div : z;
+  OpCoords c;
+  c.map = &maps[op.map];
+  if (!op.mn_major) {
+    c.x0 = op.inner_base;
+    c.y0 = op.outer_base + zz * op.z_outer + mn0;
+    c.dx = kBK;
+    c.dy = 0;
+    c.nbox = 1;
+  } else {
+    c.x0 = op.inner_base + mn0;
+    c.y0 = op.outer_base + zz * op.z_outer;
+    c.dx = 0;
+    c.dy = kBK;
+    c.nbox = rows / 64;
+  }
+  return c;
+}
+
+__device__ __forceinline__ void issue_op(const OpCoords& c, uint8_t* dst, int ks, uint64_t* bar) {
+  const int x = c.x0 + ks * c.dx, y = c.y0 + ks * c.dy;
+  if (c.nbox == 1) {
+    tma_load_2d(dst, c.map, x, y, bar);
+  } else {
+    for (int i = 0; i < c.nbox; ++i) tma_load_2d(dst + i * 8192, c.map, x + i * 64, y, bar);
+  }
+}
+
+// TMA producer (one thread): streams every (group, k-step) of one tile through
+// the ring.  `s`/`ph` are the ring position carried across tiles.  Per-operand
+// coordinates live in scalars (no runtime-indexed local arrays in the loop).
+__device__ __forceinline__ bool produce_tile(const CUtensorMap* maps, const Problem& P,
+                                             const SmemPlan& sp, const TileCoord& tc,
+                                             uint8_t* tiles, uint32_t stage_bytes, int nstages,
+                                             uint64_t* full, uint64_t* empty, int& s,
+                                             uint32_t& ph, int* status, unsigned long long lim) {
+  const int nk = P.K / kBK;
+  const uint32_t b_step = P.bn * kBK * 2;
+  for (int g = 0; g < sp.ngroups; ++g) {
+    const int j0 = sp.g_first[g], cnt = sp.g_count[g];
+    const uint32_t bytes = sp.g_bytes[g];
+    const OpCoords ca = op_coords(maps, P.a[j0], kBM, tc.tm * kBM, tc.z);
+    const OpCoords cb0 = op_coords(maps, P.b[j0], P.bn, tc.tn * P.bn, tc.z);
+    OpCoords cb1 = cb0, cb2 = cb0;
+    if (cnt > 1) cb1 = op_coords(maps, P.b[j0 + 1], P.bn, tc.tn * P.bn, tc.z);
+    if (cnt > 2) cb2 = op_coords(maps, P.b[j0 + 2], P.bn, tc.tn * P.bn, tc.z);
+    for (int ks = 0; ks < nk; ++ks) {
+      if (!mbar_wait(&empty[s], ph ^ 1, status, lim)) return false;
+      mbar_arrive_expect_tx(&full[s], bytes);
+      uint8_t* st = tiles + s * stage_bytes;
+      issue_op(ca, st, ks, &full[s]);
+      issue_op(cb0, st + kATileBytes, ks, &full[s]);
+      if (cnt > 1) issue_op(cb1, st + kATileBytes + b_step, ks, &full[s]);
+      if (cnt > 2) issue_op(cb2, st + kATileBytes + 2 * b_step, ks, &full[s]);
+      if (++s == nstages) {
+        s = 0;
+        ph ^= 1;
+      }
+    }
+  }
+  return true;
+}
+
+// Waits (bounded) until the copies of the last stages issued have landed:
+// the ring position (s, ph) is one past the last stage filled.
+__device__ __forceinline__ void drain_producer(uint64_t* full, int nstages, int s, uint32_t ph,
+                                               int filled, int* status, unsigned long long lim) {
+  for (int k = 0; k < nstages && k < filled; ++k) {
+    if (--s < 0) {
+      s = nstages - 1;
+      ph ^= 1;
+    }
+    mbar_wait(&full[s], ph, status, lim);
+  }
+}
+
+// MMA issuer (one thread): accumulates one tile into TMEM at column tmem_acc
+// (accumulator j at tmem_acc + j * bn).  Descriptors are scalars built once
+// per group; no runtime-indexed arrays in the k-step loop.
+__device__ __forceinline__ bool mma_tile(const Problem& P, const SmemPlan& sp,
+                                         uint32_t tiles_saddr, uint32_t stage_bytes, int nstages,
+                                         uint64_t* full, uint64_t* empty, uint32_t tmem_acc,
+                                         int& s, uint32_t& ph, int* status,
+                                         unsigned long long lim) {
+  const int nk = P.K / kBK;
+  const uint32_t b_step = P.bn * kBK * 2;
+  for (int g = 0; g < sp.ngroups; ++g) {
+    const int j0 = sp.g_first[g], cnt = sp.g_count[g];
+    const bool merged = sp.g_merged[g];
+    const int nmma = merged ? 1 : cnt;
+    const int a_mn = P.a[j0].mn_major;
+    const int bmn0 = P.b[j0].mn_major;
+    const int bmn1 = cnt > 1 ? P.b[j0 + 1].mn_major : bmn0;
+    const int bmn2 = cnt > 2 ? P.b[j0 + 2].mn_major : bmn0;
+    const uint32_t n0 = (merged ? cnt : 1) * P.bn;
+    const uint32_t id0 = idesc_bf16_f32(n0, a_mn, bmn0);
+    const uint32_t id1 = idesc_bf16_f32(P.bn, a_mn, bmn1);
+    const uint32_t id2 = idesc_bf16_f32(P.bn, a_mn, bmn2);
+    const uint32_t d0 = tmem_acc + j0 * P.bn, d1 = d0 + P.bn, d2 = d0 + 2 * P.bn;
+    const uint32_t bo0 = kATileBytes, bo1 = kATileBytes + b_step, bo2 = kATileBytes + 2 * b_step;
+    for (int ks = 0; ks < nk; ++ks) {
+      if (!mbar_wait(&full[s], ph, status, lim)) return false;
+      tc_fence_after();
+      const uint32_t st = tiles_saddr + s * stage_bytes;
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk) {
+        const uint32_t acc = (ks | kk) != 0;
+        const uint64_t ad = operand_desc(st, a_mn, kk);
+        umma_bf16(d0, ad, operand_desc(st + bo0, bmn0, kk), id0, acc);
+        if (nmma > 1) umma_bf16(d1, ad, operand_desc(st + bo1, bmn1, kk), id1, acc);
+        if (nmma > 2) umma_bf16(d2, ad, operand_desc(st + bo2, bmn2, kk), id2, acc);
+      }
+      umma_commit(&empty[s]);
+      if (++s == nstages) {
+        s = 0;
+        ph ^= 1;
+      }
+    }
+  }
+  return true;
+}
+
+}  // namespace ttt
