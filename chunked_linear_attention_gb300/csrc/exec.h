@@ -1,0 +1,35 @@
+// Execution helpers of the host orchestration: a per-device pool of internal
+// streams and events (fork/join of independent (batch, head) sequences), and
+// a small cache of instantiated CUDA graphs keyed by the full set of call
+// arguments, so that a repeated call replays its whole launch sequence with
+// one cudaGraphLaunch.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <functional>
+#include <vector>
+
+namespace ttt {
+
+// Internal non-blocking streams of the current device (created on first use).
+// Returns false if the pool cannot provide `n` streams.
+bool stream_pool(int n, std::vector<cudaStream_t>* out);
+
+// Fork: `n` pool streams wait for the work enqueued so far on `parent`.
+// Join: `parent` waits for everything enqueued on the pool streams.
+cudaError_t fork_streams(cudaStream_t parent, const std::vector<cudaStream_t>& kids);
+cudaError_t join_streams(cudaStream_t parent, const std::vector<cudaStream_t>& kids);
+
+// Runs `enqueue(stream)` through a cached graph when possible: on the first
+// call with a given key the launch sequence is captured on an internal stream
+// and instantiated; every call then launches the graph on `stream`.  Falls
+// back to enqueueing directly on `stream` when graphs cannot be used (the
+// stream is itself being captured, profiling is recording, or capture fails).
+// `key` must identify every argument the launch sequence depends on.
+// Returns the enqueue status code (0 = ok).
+int run_cached(const std::vector<uint64_t>& key, cudaStream_t stream,
+               const std::function<int(cudaStream_t)>& enqueue);
+
+}  // namespace ttt

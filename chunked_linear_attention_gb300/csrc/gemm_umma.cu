@@ -153,21 +153,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
-cudaError_t launch_umma_gemm(const GemmLaunch& L, cudaStream_t stream) {
+static int g_attr_done[64] = {0};
+static int g_sm_count[64] = {0};
+
+cudaError_t prepare_umma_gemm() {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  static int attr_done[64] = {0};
-  static int sm_count[64] = {0};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_done[dev]) {
+  if (!g_attr_done[dev]) {
     e = cudaFuncSetAttribute(umma_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kUmmaSmemBytes);
     if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+    e = cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    attr_done[dev] = 1;
+    g_attr_done[dev] = 1;
   }
+  return cudaSuccess;
+}
+
+cudaError_t launch_umma_gemm(const GemmLaunch& L, cudaStream_t stream) {
+  cudaError_t e = prepare_umma_gemm();
+  if (e != cudaSuccess) return e;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int* sm_count = g_sm_count;
   if (L.total_tiles <= 0) return cudaSuccess;
   const int grid = L.total_tiles < sm_count[dev] ? L.total_tiles : sm_count[dev];
   umma_gemm_kernel<<<grid, kGemmThreads, kUmmaSmemBytes, stream>>>(L);

@@ -13,6 +13,8 @@ constexpr int kUmmaSmemBytes = 227 * 1024;
 constexpr int kSimtTile = 64;
 
 cudaError_t launch_umma_gemm(const GemmLaunch& L, cudaStream_t stream);
+// One-time per-device kernel attributes (call before any stream capture).
+cudaError_t prepare_umma_gemm();
 cudaError_t launch_simt_gemm(const GemmLaunch& L, cudaStream_t stream);
 
 // ---- elementwise / reduction kernels (aux_kernels.cu)

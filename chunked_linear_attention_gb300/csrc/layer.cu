@@ -24,6 +24,7 @@
 
 #include "builder.h"
 #include "layer.h"
+#include "exec.h"
 #include "ns_cluster.h"
 #include "prof.h"
 
@@ -107,133 +108,88 @@ Problem prob0(int M, int N, int K, int Z, int nacc, int bn) {
 
 size_t layer_workspace_bytes(const LayerDims& D) { return layer_ws_layout(D, nullptr, nullptr); }
 
-int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
-                  unsigned long long wait_ns) {
+namespace {
+
+uint64_t fbits(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  return u;
+}
+
+// Everything one call enqueues, for a range [h0, h0 + nh) of (batch, head)
+// sequences.  All per-(batch, head) buffers are sliced by h0; the tensor maps
+// span whole tensors and are shared by every range.
+struct LayerPlan {
+  const LayerArgs* a;
+  const LayerDims* D;
   LayerWs w;
-  layer_ws_layout(D, &w, static_cast<char*>(a.workspace));
-  cudaStream_t st = a.stream;
+  MatSet ms[3];
+  float* mom[3];
+  TensorRef Tq, Tk, Tv, TW[3], TAq, TdH1, TdH3, TP;
+  std::vector<std::pair<int, int>> steps;
+  int* status;
+  unsigned long long wait_ns;
+};
+
+#define TTT_CK(x)                      \
+  do {                                 \
+    if ((x) != cudaSuccess) return -6; \
+  } while (0)
+
+int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStream_t st) {
+  const LayerArgs& a = *L.a;
+  const LayerDims& D = *L.D;
+  const LayerWs& w = L.w;
   const bool tc = D.bf16;
   const int BH = D.B * D.H, d = D.d, m = D.m, b = D.chunk, N = D.N;
   const long long dm = (long long)d * m;
-  const int nc = N / b;
   const int rows_of[3] = {m, m, d}, cols_of[3] = {d, d, m};
   const bool muon = D.muon_steps > 0;
-  cudaError_t ce;
-#define TTT_CK(x)                   \
-  do {                              \
-    ce = (x);                       \
-    if (ce != cudaSuccess) return -6; \
-  } while (0)
-
-  // ---- state init
-  MatSet ms[3];
-  for (int s = 0; s < 3; ++s) {
-    ms[s].init = a.W[kPub[s]];
-    ms[s].init_per_batch = a.w_per_batch;
-    ms[s].master = a.Wf[kPub[s]];
-    ms[s].work = tc ? w.Wb[s] : nullptr;
-    ms[s].rows = rows_of[s];
-    ms[s].cols = cols_of[s];
-    ProfScope ps(PT_INIT, st, 0.0, (double)BH * rows_of[s] * cols_of[s] * (4 + 4 + (tc ? 2 : 0)));
-    TTT_CK(launch_init_weights(ms[s], D.B, D.H, st));
-  }
-  float* mom[3];
-  for (int s = 0; s < 3; ++s) {
-    if (a.momentum)
-      mom[s] = a.momentum + (long long)kPub[s] * BH * dm;
-    else
-      mom[s] = w.M ? w.M + (long long)s * BH * dm : nullptr;
-  }
-  if (!a.momentum && w.M) {
-    ProfScope ps(PT_INIT, st, 0.0, 3.0 * BH * dm * 4);
-    TTT_CK(launch_copy_f32(w.M, nullptr, 3LL * BH * dm, st));
-  }
-  {
-    ProfScope ps(PT_INIT, st, 0.0, 3.0 * BH * 4);
-    TTT_CK(launch_copy_f32(w.normsq, nullptr, 3LL * BH, st));
-  }
-  for (int s = 0; s < 3; ++s) {
-    float* u_slot = w.U + (long long)s * BH * dm;
-    ms[s].update = (!muon && mom[s]) ? mom[s] : u_slot;
-  }
-
-  // ---- tensor views
-  const int wb16 = tc ? 1 : 0;
   const size_t es = tc ? 2 : 4;
-  TensorRef Tq{a.q, wb16, (long long)BH * N, d};
-  TensorRef Tk{a.k, wb16, (long long)BH * N, d};
-  TensorRef Tv{a.v, wb16, (long long)BH * N, d};
-  TensorRef TW[3];
-  for (int s = 0; s < 3; ++s)
-    TW[s] = TensorRef{tc ? w.Wb[s] : static_cast<const void*>(a.Wf[kPub[s]]), wb16,
-                      (long long)BH * rows_of[s], cols_of[s]};
-  TensorRef TAq{w.Aq, wb16, (long long)BH * b, m};
-  TensorRef TdH1{w.dH1, wb16, (long long)BH * b, m};
-  TensorRef TdH3{w.dH3, wb16, (long long)BH * b, m};
-  TensorRef TP{w.P, wb16, (long long)BH * b, m};
-
-  MapCache cache;
-  LaunchBuilder LB(tc, &cache, status, wait_ns);
+  const size_t ios = tc ? 2 : 4;
+  auto offs = [&](void* p, long long elems) -> void* {
+    return p ? static_cast<char*>(p) + elems * (long long)es : nullptr;
+  };
+  LaunchBuilder LB(tc, &cache, L.status, L.wait_ns);
   const int BM = LB.bm();
+  const long long bm_h = (long long)b * m;   // activation elements per (batch, head)
 
-  // ---- step schedule: (apply chunk, update chunk), -1 = none
-  std::vector<std::pair<int, int>> steps;
-  if (D.mode == 0) {
-    for (int c = 0; c < nc; ++c) steps.push_back({c, c});
-  } else {
-    std::vector<int> pending;
-    for (int c = 0; c < nc; ++c) {
-      const bool upd = D.mode != 3 || (a.update_chunks && a.update_chunks[c]);
-      if (upd) {
-        while (pending.size() > 1) {
-          steps.push_back({pending.front(), -1});
-          pending.erase(pending.begin());
-        }
-        steps.push_back({pending.empty() ? -1 : pending.front(), c});
-        pending.assign(1, c);
-      } else {
-        pending.push_back(c);
-      }
-    }
-    for (int p : pending) steps.push_back({p, -1});
-  }
-
-  for (const auto& stp : steps) {
+  for (const auto& stp : L.steps) {
     const int ap = stp.first, up = stp.second;
     // ---------------- PROJ
     if (up >= 0) {
       const int bn = LB.choose_bn(m, 3);
-      Problem p = prob0(b, m, d, BH, 3, bn);
-      p.a[0] = LB.op(Tk, 0, up * b, N, BM);
-      p.b[0] = LB.op(TW[0], 0, 0, m, bn);
+      Problem p = prob0(b, m, d, nh, 3, bn);
+      p.a[0] = LB.op(L.Tk, 0, h0 * N + up * b, N, BM);
+      p.b[0] = LB.op(L.TW[0], 0, h0 * m, m, bn);
       p.a[1] = p.a[0];
-      p.b[1] = LB.op(TW[1], 0, 0, m, bn);
-      p.a[2] = LB.op(Tv, 0, up * b, N, BM);
-      p.b[2] = LB.op(TW[2], 1, 0, d, bn);  // W2 [d, m]: K = d rows, N = m contiguous
+      p.b[1] = LB.op(L.TW[1], 0, h0 * m, m, bn);
+      p.a[2] = LB.op(L.Tv, 0, h0 * N + up * b, N, BM);
+      p.b[2] = LB.op(L.TW[2], 1, h0 * d, d, bn);  // W2 [d, m]: K = d rows, N = m contiguous
       p.a_shared = 1 << 1;
       p.epi.kind = EPI_PROJ_K;
-      p.epi.out[0] = w.dH1;
-      p.epi.out[1] = w.dH3;
-      p.epi.out[2] = w.P;
+      p.epi.out[0] = offs(w.dH1, h0 * bm_h);
+      p.epi.out[1] = offs(w.dH3, h0 * bm_h);
+      p.epi.out[2] = offs(w.P, h0 * bm_h);
       p.epi.out_ld = m;
-      p.epi.out_z = (long long)b * m;
-      p.epi.eta = a.eta;
+      p.epi.out_z = bm_h;
+      p.epi.eta = a.eta + (long long)h0 * N;
       p.epi.eta_z = N;
       p.epi.eta_row0 = (long long)up * b;
       LB.add(p);
     }
     if (ap >= 0) {
       const int bn = LB.choose_bn(m, 2);
-      Problem p = prob0(b, m, d, BH, 2, bn);
-      p.a[0] = LB.op(Tq, 0, ap * b, N, BM);
-      p.b[0] = LB.op(TW[0], 0, 0, m, bn);
+      Problem p = prob0(b, m, d, nh, 2, bn);
+      p.a[0] = LB.op(L.Tq, 0, h0 * N + ap * b, N, BM);
+      p.b[0] = LB.op(L.TW[0], 0, h0 * m, m, bn);
       p.a[1] = p.a[0];
-      p.b[1] = LB.op(TW[1], 0, 0, m, bn);
+      p.b[1] = LB.op(L.TW[1], 0, h0 * m, m, bn);
       p.a_shared = 1 << 1;
       p.epi.kind = EPI_PROJ_Q;
-      p.epi.out[0] = w.Aq;
+      p.epi.out[0] = offs(w.Aq, h0 * bm_h);
       p.epi.out_ld = m;
-      p.epi.out_z = (long long)b * m;
+      p.epi.out_z = bm_h;
       LB.add(p);
     }
     if (!LB.ok()) return -4;
@@ -244,35 +200,35 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
       for (int s = 0; s < 3; ++s) {
         const int M = rows_of[s], Nn = cols_of[s];
         const int bn = LB.choose_bn(Nn, 1);
-        Problem p = prob0(M, Nn, b, BH, 1, bn);
+        Problem p = prob0(M, Nn, b, nh, 1, bn);
         if (s < 2) {  // g1 = dH1^T K, g3 = dH3^T K  [m, d]
-          p.a[0] = LB.op(s == 0 ? TdH1 : TdH3, 1, 0, b, 64);
-          p.b[0] = LB.op(Tk, 1, up * b, N, 64);
+          p.a[0] = LB.op(s == 0 ? L.TdH1 : L.TdH3, 1, h0 * b, b, 64);
+          p.b[0] = LB.op(L.Tk, 1, h0 * N + up * b, N, 64);
         } else {      // g2 = V^T P  [d, m]
-          p.a[0] = LB.op(Tv, 1, up * b, N, 64);
-          p.b[0] = LB.op(TP, 1, 0, b, 64);
+          p.a[0] = LB.op(L.Tv, 1, h0 * N + up * b, N, 64);
+          p.b[0] = LB.op(L.TP, 1, h0 * b, b, 64);
         }
         p.epi.kind = EPI_GRAD;
         p.epi.out_ld = Nn;
         p.epi.out_z = dm;
-        p.epi.mom = mom[s];
+        p.epi.mom = L.mom[s] ? L.mom[s] + (long long)h0 * dm : nullptr;
         p.epi.a = D.beta;
         if (muon) {
-          p.epi.out[1] = static_cast<char*>(w.X[0]) + (size_t)s * BH * dm * es;
-          p.epi.normsq_out = w.normsq + (long long)s * BH;
-        } else if (!mom[s]) {
-          p.epi.out[0] = w.U + (long long)s * BH * dm;
+          p.epi.out[1] = offs(w.X[0], (long long)s * BH * dm + h0 * dm);
+          p.epi.normsq_out = w.normsq + (long long)s * BH + h0;
+        } else if (!L.mom[s]) {
+          p.epi.out[0] = w.U + (long long)s * BH * dm + h0 * dm;
         }
         LB.add(p);
       }
     }
     if (ap >= 0) {
       const int bn = LB.choose_bn(d, 1);
-      Problem p = prob0(b, d, m, BH, 1, bn);
-      p.a[0] = LB.op(TAq, 0, 0, b, BM);
-      p.b[0] = LB.op(TW[2], 0, 0, d, bn);  // W2 [d, m]: N = d rows, K = m contiguous
+      Problem p = prob0(b, d, m, nh, 1, bn);
+      p.a[0] = LB.op(L.TAq, 0, h0 * b, b, BM);
+      p.b[0] = LB.op(L.TW[2], 0, h0 * d, d, bn);  // W2 [d, m]: N = d rows, K = m contiguous
       p.epi.kind = EPI_OUT;
-      p.epi.out[0] = a.out;
+      p.epi.out[0] = static_cast<char*>(a.out) + (long long)h0 * N * d * (long long)ios;
       p.epi.out_ld = d;
       p.epi.out_z = (long long)N * d;
       p.epi.out_row0 = (long long)ap * b;
@@ -294,21 +250,24 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
       na.U = w.U;
       na.normsq = w.normsq;
       for (int s = 0; s < 3; ++s) {
-        na.W[s] = ms[s].master;
-        na.Wb[s] = ms[s].work;
+        na.W[s] = L.ms[s].master;
+        na.Wb[s] = L.ms[s].work;
       }
       na.BH = BH;
+      na.h0 = h0;
+      na.nh = nh;
       na.d = d;
       na.steps = D.muon_steps;
       na.l2norm = D.l2norm;
       na.ns[0] = D.ns[0];
       na.ns[1] = D.ns[1];
       na.ns[2] = D.ns[2];
-      const int rc = launch_ns_cluster(cache, na, status, wait_ns, st);
+      const int rc = launch_ns_cluster(cache, na, L.status, L.wait_ns, st);
       if (rc < 0) return rc;
       fused_update = rc == 0;
     }
     if (muon && !fused_update) {
+      if (h0 != 0 || nh != BH) return -4;   // per-product path runs over all sequences
       const int sdim = std::min(d, m);
       // groups of equally shaped slots: {0,1,2} if square, else {0,1} and {2}
       int groups[2][2];  // first slot, count
@@ -318,6 +277,7 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
       } else {
         groups[0][0] = 0; groups[0][1] = 2; groups[1][0] = 2; groups[1][1] = 1; ng = 2;
       }
+      const int wb16 = tc ? 1 : 0;
       for (int t = 0; t < D.muon_steps; ++t) {
         const int in = t & 1;
         const bool last = t == D.muon_steps - 1;
@@ -326,8 +286,7 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
           const int s0 = groups[g][0], cnt = groups[g][1];
           const int R = rows_of[s0], C = cols_of[s0];
           const int Z = cnt * BH;
-          TensorRef TX{static_cast<char*>(w.X[in]) + (size_t)s0 * BH * dm * es, wb16,
-                       (long long)Z * R, C};
+          TensorRef TX{offs(w.X[in], (long long)s0 * BH * dm), wb16, (long long)Z * R, C};
           const int bn = LB.choose_bn(sdim, 1);
           Problem p = prob0(sdim, sdim, std::max(R, C), Z, 1, bn);
           if (R <= C) {
@@ -338,7 +297,7 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
             p.b[0] = LB.op(TX, 1, 0, R, 64);
           }
           p.epi.kind = EPI_NS_GRAM;
-          p.epi.out[0] = static_cast<char*>(w.G) + (size_t)s0 * BH * sdim * sdim * es;
+          p.epi.out[0] = offs(w.G, (long long)s0 * BH * sdim * sdim);
           p.epi.out_ld = sdim;
           p.epi.out_z = (long long)sdim * sdim;
           p.epi.first = t == 0;
@@ -352,15 +311,15 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
         for (int g = 0; g < ng; ++g) {
           const int s0 = groups[g][0], cnt = groups[g][1];
           const int Z = cnt * BH;
-          TensorRef TG{static_cast<char*>(w.G) + (size_t)s0 * BH * sdim * sdim * es, wb16,
-                       (long long)Z * sdim, sdim};
+          TensorRef TG{offs(w.G, (long long)s0 * BH * sdim * sdim), wb16, (long long)Z * sdim,
+                       sdim};
           const int bn = LB.choose_bn(sdim, 1);
           Problem p = prob0(sdim, sdim, sdim, Z, 1, bn);
           p.a[0] = LB.op(TG, 0, 0, sdim, BM);
           p.b[0] = LB.op(TG, 0, 0, sdim, bn);
           p.epi.kind = EPI_NS_POLY;
           p.epi.in0 = TG.ptr;
-          p.epi.out[0] = static_cast<char*>(w.Bm) + (size_t)s0 * BH * sdim * sdim * es;
+          p.epi.out[0] = offs(w.Bm, (long long)s0 * BH * sdim * sdim);
           p.epi.out_ld = sdim;
           p.epi.out_z = (long long)sdim * sdim;
           p.epi.b = D.ns[1];
@@ -374,10 +333,9 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
           const int s0 = groups[g][0], cnt = groups[g][1];
           const int R = rows_of[s0], C = cols_of[s0];
           const int Z = cnt * BH;
-          TensorRef TX{static_cast<char*>(w.X[in]) + (size_t)s0 * BH * dm * es, wb16,
-                       (long long)Z * R, C};
-          TensorRef TB{static_cast<char*>(w.Bm) + (size_t)s0 * BH * sdim * sdim * es, wb16,
-                       (long long)Z * sdim, sdim};
+          TensorRef TX{offs(w.X[in], (long long)s0 * BH * dm), wb16, (long long)Z * R, C};
+          TensorRef TB{offs(w.Bm, (long long)s0 * BH * sdim * sdim), wb16, (long long)Z * sdim,
+                       sdim};
           const int bn = LB.choose_bn(C, 1);
           Problem p = prob0(R, C, sdim, Z, 1, bn);
           if (R <= C) {
@@ -392,7 +350,7 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
           if (last)
             p.epi.out[1] = w.U + (long long)s0 * BH * dm;
           else
-            p.epi.out[0] = static_cast<char*>(w.X[in ^ 1]) + (size_t)s0 * BH * dm * es;
+            p.epi.out[0] = offs(w.X[in ^ 1], (long long)s0 * BH * dm);
           p.epi.out_ld = C;
           p.epi.out_z = dm;
           p.epi.a = D.ns[0];
@@ -408,13 +366,155 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
 
     // ---------------- NORM
     if (!fused_update) {
-      ProfScope ps(PT_NORM, st, 0.0, 3.0 * BH * dm * (4 + 4 + 4 + (tc ? 2 : 0)));
-      TTT_CK(launch_update_normalize(ms, 3, BH, D.l2norm, muon ? w.normsq : nullptr,
+      MatSet part[3];
+      for (int s = 0; s < 3; ++s) {
+        const long long rc = (long long)rows_of[s] * cols_of[s];
+        part[s] = L.ms[s];
+        part[s].master = L.ms[s].master + h0 * rc;
+        part[s].work = L.ms[s].work ? static_cast<char*>(L.ms[s].work) + h0 * rc * 2 : nullptr;
+        part[s].update = L.ms[s].update + h0 * rc;
+      }
+      ProfScope ps(PT_NORM, st, 0.0, 3.0 * nh * dm * (4 + 4 + 4 + (tc ? 2 : 0)));
+      TTT_CK(launch_update_normalize(part, 3, nh, D.l2norm, muon ? w.normsq : nullptr,
                                      muon ? 3 * BH : 0, st));
     }
   }
-#undef TTT_CK
   return 0;
+}
+
+// Sequences run one stream each (so that one sequence's latency-bound Muon
+// overlaps other sequences' projections) when the whole update of a sequence
+// can be enqueued per sequence: the bf16 path with square matrices under the
+// cluster Newton-Schulz kernel, or without Muon.
+bool per_sequence_streams(const LayerDims& D) {
+  if (!D.bf16 || D.B * D.H < 2) return false;
+  if (D.muon_steps == 0) return true;
+  return D.d == D.m && prepare_ns_cluster(D.d);
+}
+
+int enqueue_all(LayerPlan& L, cudaStream_t st) {
+  const LayerArgs& a = *L.a;
+  const LayerDims& D = *L.D;
+  const LayerWs& w = L.w;
+  const bool tc = D.bf16;
+  const int BH = D.B * D.H;
+  const long long dm = (long long)D.d * D.m;
+  const int rows_of[3] = {D.m, D.m, D.d}, cols_of[3] = {D.d, D.d, D.m};
+  for (int s = 0; s < 3; ++s) {
+    ProfScope ps(PT_INIT, st, 0.0,
+                 (double)BH * rows_of[s] * cols_of[s] * (4 + 4 + (tc ? 2 : 0)));
+    TTT_CK(launch_init_weights(L.ms[s], D.B, D.H, st));
+  }
+  if (!a.momentum && w.M) {
+    ProfScope ps(PT_INIT, st, 0.0, 3.0 * BH * dm * 4);
+    TTT_CK(launch_copy_f32(w.M, nullptr, 3LL * BH * dm, st));
+  }
+  {
+    ProfScope ps(PT_INIT, st, 0.0, 3.0 * BH * 4);
+    TTT_CK(launch_copy_f32(w.normsq, nullptr, 3LL * BH, st));
+  }
+  MapCache cache;
+  std::vector<cudaStream_t> kids;
+  if (per_sequence_streams(D) && stream_pool(BH, &kids)) {
+    TTT_CK(fork_streams(st, kids));
+    for (int h = 0; h < BH; ++h) {
+      const int rc = enqueue_range(L, cache, h, 1, kids[h]);
+      if (rc != 0) return rc;
+    }
+    TTT_CK(join_streams(st, kids));
+    return 0;
+  }
+  return enqueue_range(L, cache, 0, BH, st);
+}
+
+#undef TTT_CK
+
+}  // namespace
+
+int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
+                  unsigned long long wait_ns) {
+  LayerPlan L;
+  L.a = &a;
+  L.D = &D;
+  L.status = status;
+  L.wait_ns = wait_ns;
+  layer_ws_layout(D, &L.w, static_cast<char*>(a.workspace));
+  const LayerWs& w = L.w;
+  const bool tc = D.bf16;
+  const int BH = D.B * D.H, d = D.d, m = D.m, b = D.chunk, N = D.N;
+  const long long dm = (long long)d * m;
+  const int nc = N / b;
+  const int rows_of[3] = {m, m, d}, cols_of[3] = {d, d, m};
+  const bool muon = D.muon_steps > 0;
+
+  for (int s = 0; s < 3; ++s) {
+    L.ms[s].init = a.W[kPub[s]];
+    L.ms[s].init_per_batch = a.w_per_batch;
+    L.ms[s].master = a.Wf[kPub[s]];
+    L.ms[s].work = tc ? w.Wb[s] : nullptr;
+    L.ms[s].rows = rows_of[s];
+    L.ms[s].cols = cols_of[s];
+    if (a.momentum)
+      L.mom[s] = a.momentum + (long long)kPub[s] * BH * dm;
+    else
+      L.mom[s] = w.M ? w.M + (long long)s * BH * dm : nullptr;
+    float* u_slot = w.U + (long long)s * BH * dm;
+    L.ms[s].update = (!muon && L.mom[s]) ? L.mom[s] : u_slot;
+  }
+  const int wb16 = tc ? 1 : 0;
+  L.Tq = TensorRef{a.q, wb16, (long long)BH * N, d};
+  L.Tk = TensorRef{a.k, wb16, (long long)BH * N, d};
+  L.Tv = TensorRef{a.v, wb16, (long long)BH * N, d};
+  for (int s = 0; s < 3; ++s)
+    L.TW[s] = TensorRef{tc ? w.Wb[s] : static_cast<const void*>(a.Wf[kPub[s]]), wb16,
+                        (long long)BH * rows_of[s], cols_of[s]};
+  L.TAq = TensorRef{w.Aq, wb16, (long long)BH * b, m};
+  L.TdH1 = TensorRef{w.dH1, wb16, (long long)BH * b, m};
+  L.TdH3 = TensorRef{w.dH3, wb16, (long long)BH * b, m};
+  L.TP = TensorRef{w.P, wb16, (long long)BH * b, m};
+
+  // step schedule: (apply chunk, update chunk), -1 = none
+  std::vector<uint64_t> flagbits((nc + 63) / 64, 0);
+  if (D.mode == 0) {
+    for (int c = 0; c < nc; ++c) L.steps.push_back({c, c});
+  } else {
+    std::vector<int> pending;
+    for (int c = 0; c < nc; ++c) {
+      const bool upd = D.mode != 3 || (a.update_chunks && a.update_chunks[c]);
+      if (upd) flagbits[c / 64] |= 1ull << (c % 64);
+      if (upd) {
+        while (pending.size() > 1) {
+          L.steps.push_back({pending.front(), -1});
+          pending.erase(pending.begin());
+        }
+        L.steps.push_back({pending.empty() ? -1 : pending.front(), c});
+        pending.assign(1, c);
+      } else {
+        pending.push_back(c);
+      }
+    }
+    for (int p : pending) L.steps.push_back({p, -1});
+  }
+
+  // every argument the launch sequence depends on
+  std::vector<uint64_t> key = {
+      0x7474746c61796572ull,  // call kind
+      (uint64_t)a.q, (uint64_t)a.k, (uint64_t)a.v, (uint64_t)a.eta,
+      (uint64_t)a.W[0], (uint64_t)a.W[1], (uint64_t)a.W[2], (uint64_t)a.w_per_batch,
+      (uint64_t)a.out, (uint64_t)a.Wf[0], (uint64_t)a.Wf[1], (uint64_t)a.Wf[2],
+      (uint64_t)a.momentum, (uint64_t)a.workspace,
+      (uint64_t)D.B, (uint64_t)D.H, (uint64_t)D.N, (uint64_t)D.d, (uint64_t)D.m,
+      (uint64_t)D.chunk, (uint64_t)D.bf16, (uint64_t)D.mode, (uint64_t)D.l2norm,
+      (uint64_t)D.muon_steps, fbits(D.beta),
+      fbits(D.ns[0]), fbits(D.ns[1]),
+      fbits(D.ns[2]), (uint64_t)status, (uint64_t)wait_ns};
+  key.insert(key.end(), flagbits.begin(), flagbits.end());
+  // one-time device setup outside any capture
+  if (tc) {
+    if (prepare_umma_gemm() != cudaSuccess) return -6;
+    if (muon && d == m) prepare_ns_cluster(d);
+  }
+  return run_cached(key, a.stream, [&](cudaStream_t s) { return enqueue_all(L, s); });
 }
 
 }  // namespace ttt

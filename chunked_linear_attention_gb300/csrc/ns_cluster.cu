@@ -39,6 +39,7 @@ struct NsLaunch {
   float* W[3];                // fp32 state per slot (W1, W3, W2), [B*H][d*d]
   void* Wb[3];                // bf16 operand copies per slot
   int BH, d, steps, cs, l2norm;
+  int h0, nh;                 // (batch, head) range of this launch
   int* status;
   unsigned long long wait_limit_ns;
 };
@@ -84,7 +85,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = (int)cluster_ctarank();
-  const int z = blockIdx.x / L.cs;   // matrix index (slot-major over B*H)
+  // matrix index (slot-major over B*H) of this cluster
+  const int zl = blockIdx.x / L.cs;
+  const int z = (zl / L.nh) * L.BH + L.h0 + (zl % L.nh);
 
   uint32_t stage_bytes = 0;
   {
@@ -284,6 +287,14 @@ static bool cluster_fits(int dev, int cs) {
   return c == 1;
 }
 
+bool prepare_ns_cluster(int d) {
+  int cs = 0, bn = 0;
+  if (!ns_cluster_applicable(d, &cs, &bn)) return false;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  return cluster_fits(dev, cs);
+}
+
 int launch_ns_cluster(MapCache& cache, const NsArgs& a, int* status, unsigned long long wait_ns,
                       cudaStream_t stream) {
   int cs = 0, bn = 0;
@@ -361,6 +372,8 @@ int launch_ns_cluster(MapCache& cache, const NsArgs& a, int* status, unsigned lo
     L.Wb[s] = a.Wb[s];
   }
   L.BH = a.BH;
+  L.h0 = a.h0;
+  L.nh = a.nh;
   L.d = d;
   L.steps = a.steps;
   L.cs = cs;
@@ -374,14 +387,14 @@ int launch_ns_cluster(MapCache& cache, const NsArgs& a, int* status, unsigned lo
   attr[0].val.clusterDim.x = cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(Z * cs, 1, 1);
+  cfg.gridDim = dim3(3 * a.nh * cs, 1, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = kUmmaSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const double r = d, c = d;
-  const double flops = (double)Z * a.steps * (4 * r * c * c + 2 * c * c * c);
+  const double flops = 3.0 * a.nh * a.steps * (4 * r * c * c + 2 * c * c * c);
   ProfScope ps(PT_MUON, stream, flops, 0.0);
   if (cudaLaunchKernelEx(&cfg, ns_cluster_kernel, L) != cudaSuccess) return -6;
   return 0;

@@ -16,11 +16,16 @@ struct NsArgs {
   float* W[3];       // fp32 state per slot (W1, W3, W2)
   void* Wb[3];       // bf16 operand copies per slot
   int BH, d, steps, l2norm;
+  int h0, nh;        // (batch, head) range handled by this launch: [h0, h0 + nh)
   float ns[3];
 };
 
 // True if the cluster kernel handles d x d matrices; gives cluster size and N tile.
 bool ns_cluster_applicable(int d, int* cs, int* bn);
+
+// One-time per-device setup for d x d matrices (call before any stream
+// capture); false if the cluster kernel cannot run them on this device.
+bool prepare_ns_cluster(int d);
 
 // Enqueues the whole Muon + update + normalisation for all matrices.
 // Returns 0 on success, 1 if this device/shape cannot use the cluster kernel

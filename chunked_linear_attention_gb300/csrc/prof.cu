@@ -32,6 +32,13 @@ const char* kTagKernel[PT_COUNT] = {
 
 }  // namespace
 
+bool prof_recording() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return g_on;
+}
+
+void prof_count_launches(size_t n) { g_launches.fetch_add(n); }
+
 ProfScope::ProfScope(int tag, cudaStream_t s, double flops, double bytes) : idx_(-1), s_(s) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (!g_on) return;

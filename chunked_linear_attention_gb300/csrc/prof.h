@@ -23,6 +23,12 @@ enum ProfTag : int {
   PT_COUNT
 };
 
+// True while a profile is recording (launch sequences are then not cached as
+// graphs, so every launch gets its events).
+bool prof_recording();
+// Adds launches that ran without a ProfScope (graph replays).
+void prof_count_launches(size_t n);
+
 // Records (when profiling) an event before the launch; the destructor
 // records the one after and counts the launch.
 class ProfScope {

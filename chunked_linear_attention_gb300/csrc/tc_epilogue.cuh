@@ -2,7 +2,7 @@
 // fused epilogue of epilogue.cuh, with memory traffic shaped for the GPU:
 //
 //   * each epilogue warp owns 32 rows (its TMEM lane quarter) and the tile's
-//     columns, processed in blocks of 32 columns;
+//     columns, processed in blocks of kBW columns;
 //   * per-row scalars (eta, the Newton-Schulz scale) are read once per tile,
 //     before waiting for the accumulator;
 //   * input tiles (momentum, Newton-Schulz iterates) are fetched with
@@ -10,8 +10,8 @@
 //     padded per-warp staging buffer in shared memory;
 //   * outputs go back through the same buffer and leave as coalesced 16-byte
 //     stores that cover whole 64/128-byte row segments.
-// The staging buffer holds 32 rows x 33 floats (the pad makes both the
-// row-wise and the chunk-wise accesses bank-conflict free).
+// The staging buffer holds 32 rows x (kBW + 1) floats (the pad spreads both
+// the row-wise and the chunk-wise accesses over the banks).
 #pragma once
 
 #include "common.cuh"
@@ -20,24 +20,26 @@
 
 namespace ttt {
 
-constexpr int kStageStride = 33;                      // floats per staged row
+constexpr int kBW = 16;                               // columns per epilogue block
+constexpr int kStageStride = kBW + 1;                 // floats per staged row (padded)
 constexpr int kStageFloats = 32 * kStageStride;       // per warp
 // all epilogue warps' staging buffers, rounded up to keep the stage ring 1 KB aligned
 constexpr int kStagingBytes = (kEpiWarps * kStageFloats * 4 + 1023) / 1024 * 1024;
 
-// 32 x 32 block of T starting at (row0, col0) of a row-major matrix with
-// leading dimension ld; one warp, coalesced.  bf16: 4 x 16 B per thread
-// (8 rows x 4 chunks per instruction); fp32: 8 x 16 B (4 rows x 8 chunks).
+// 32 x kBW block of T starting at `base` of a row-major matrix with leading
+// dimension ld; one warp, coalesced 16-byte accesses.
 template <typename T>
 struct BlockRegs {
-  uint4 r[sizeof(T) == 2 ? 4 : 8];
+  static constexpr int kCPR = kBW * (int)sizeof(T) / 16;   // 16-byte chunks per row
+  static constexpr int kRPI = 32 / kCPR;                    // rows per warp instruction
+  uint4 r[32 / kRPI];
 };
 
 template <typename T>
 __device__ __forceinline__ void block_load(const T* base, long long ld, int rows_valid,
                                            BlockRegs<T>& g, int lane) {
-  constexpr int kCPR = sizeof(T) == 2 ? 4 : 8;               // chunks per row
-  constexpr int kRPI = 32 / kCPR;                            // rows per instruction
+  constexpr int kCPR = BlockRegs<T>::kCPR;
+  constexpr int kRPI = BlockRegs<T>::kRPI;
 #pragma unroll
   for (int i = 0; i < 32 / kRPI; ++i) {
     const int r = i * kRPI + lane / kCPR;
@@ -52,8 +54,8 @@ __device__ __forceinline__ void block_load(const T* base, long long ld, int rows
 // Coalesced registers -> staging (as fp32).
 template <typename T>
 __device__ __forceinline__ void block_to_stage(const BlockRegs<T>& g, float* stage, int lane) {
-  constexpr int kCPR = sizeof(T) == 2 ? 4 : 8;
-  constexpr int kRPI = 32 / kCPR;
+  constexpr int kCPR = BlockRegs<T>::kCPR;
+  constexpr int kRPI = BlockRegs<T>::kRPI;
   constexpr int kEPC = 16 / sizeof(T);  // elements per chunk
 #pragma unroll
   for (int i = 0; i < 32 / kRPI; ++i) {
@@ -75,8 +77,8 @@ __device__ __forceinline__ void block_to_stage(const BlockRegs<T>& g, float* sta
 template <typename T>
 __device__ __forceinline__ void stage_to_global(const float* stage, T* base, long long ld,
                                                 int rows_valid, int lane) {
-  constexpr int kCPR = sizeof(T) == 2 ? 4 : 8;
-  constexpr int kRPI = 32 / kCPR;
+  constexpr int kCPR = BlockRegs<T>::kCPR;
+  constexpr int kRPI = BlockRegs<T>::kRPI;
   constexpr int kEPC = 16 / sizeof(T);
 #pragma unroll
   for (int i = 0; i < 32 / kRPI; ++i) {
@@ -95,19 +97,19 @@ __device__ __forceinline__ void stage_to_global(const float* stage, T* base, lon
   }
 }
 
-// This thread's row of 32 values: registers -> staging row / staging row -> registers.
-__device__ __forceinline__ void row_to_stage(const float (&v)[32], float* stage, int lane) {
+// This thread's row of kBW values: registers -> staging row / staging row -> registers.
+__device__ __forceinline__ void row_to_stage(const float (&v)[kBW], float* stage, int lane) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j) stage[lane * kStageStride + j] = v[j];
+  for (int j = 0; j < kBW; ++j) stage[lane * kStageStride + j] = v[j];
 }
-__device__ __forceinline__ void stage_to_row(const float* stage, float (&v)[32], int lane) {
+__device__ __forceinline__ void stage_to_row(const float* stage, float (&v)[kBW], int lane) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = stage[lane * kStageStride + j];
+  for (int j = 0; j < kBW; ++j) v[j] = stage[lane * kStageStride + j];
 }
 
 // Writes a row-held block through the staging buffer to global memory.
 template <typename T>
-__device__ __forceinline__ void store_rows(const float (&v)[32], float* stage, T* base, long long ld,
+__device__ __forceinline__ void store_rows(const float (&v)[kBW], float* stage, T* base, long long ld,
                                            int rows_valid, int lane) {
   row_to_stage(v, stage, lane);
   __syncwarp();
@@ -141,14 +143,14 @@ __device__ __noinline__ float tc_epilogue_blocks(const Problem& P, int tn, uint3
   };
   prefetch(c_begin);
   float sumsq = 0.f;
-  for (int c0 = c_begin; c0 < c_end; c0 += 32) {
-    float v0[32];
-    float v1[kAcc > 1 ? 32 : 1];
-    float v2[kAcc > 2 ? 32 : 1];
-    float x[(kInBf16 || kInF32) ? 32 : 1];
-    tmem_ld32(tl + c0, v0);
-    if constexpr (kAcc > 1) tmem_ld32(tl + bn + c0, v1);
-    if constexpr (kAcc > 2) tmem_ld32(tl + 2 * bn + c0, v2);
+  for (int c0 = c_begin; c0 < c_end; c0 += kBW) {
+    float v0[kBW];
+    float v1[kAcc > 1 ? kBW : 1];
+    float v2[kAcc > 2 ? kBW : 1];
+    float x[(kInBf16 || kInF32) ? kBW : 1];
+    tmem_ld16_nowait(tl + c0, v0);
+    if constexpr (kAcc > 1) tmem_ld16_nowait(tl + bn + c0, v1);
+    if constexpr (kAcc > 2) tmem_ld16_nowait(tl + 2 * bn + c0, v2);
     const int gcol = tn * bn + c0;
     const bool active = rows_valid > 0 && gcol < P.N;
     if constexpr (kInBf16 || kInF32) {
@@ -160,22 +162,22 @@ __device__ __noinline__ float tc_epilogue_blocks(const Problem& P, int tn, uint3
         __syncwarp();
       }
     }
-    if (c0 + 32 < c_end) prefetch(c0 + 32);
-    tmem_wait32(v0);
-    if constexpr (kAcc > 1) tmem_wait32(v1);
-    if constexpr (kAcc > 2) tmem_wait32(v2);
+    if (c0 + kBW < c_end) prefetch(c0 + kBW);
+    tmem_wait_bind(v0);
+    if constexpr (kAcc > 1) tmem_wait_bind(v1);
+    if constexpr (kAcc > 2) tmem_wait_bind(v2);
     if (!active) continue;
     const long long off = tile_base + gcol;
     if constexpr (KIND == EPI_STORE_F32) {
       store_rows<float>(v0, stage, static_cast<float*>(e.out[0]) + off, e.out_ld, rows_valid, lane);
     } else if constexpr (KIND == EPI_PROJ_Q) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v0[i] = v0[i] * sigmoid_f(v0[i]) * v1[i];
+      for (int i = 0; i < kBW; ++i) v0[i] = v0[i] * sigmoid_f(v0[i]) * v1[i];
       store_rows<__nv_bfloat16>(v0, stage, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
                                 rows_valid, lane);
     } else if constexpr (KIND == EPI_PROJ_K) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < kBW; ++i) {
         const float h1 = v0[i], h3 = v1[i];
         const float s = sigmoid_f(h1);
         const float sl = h1 * s;
@@ -193,7 +195,7 @@ __device__ __noinline__ float tc_epilogue_blocks(const Problem& P, int tn, uint3
     } else if constexpr (KIND == EPI_GRAD) {
       if (has_mom) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v0[i] = e.a * x[i] + v0[i];
+        for (int i = 0; i < kBW; ++i) v0[i] = e.a * x[i] + v0[i];
         store_rows<float>(v0, stage, e.mom + off, e.out_ld, rows_valid, lane);
       }
       if (e.out[0])
@@ -204,7 +206,7 @@ __device__ __noinline__ float tc_epilogue_blocks(const Problem& P, int tn, uint3
                                   e.out_ld, rows_valid, lane);
         if (lane < rows_valid) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) sumsq += v0[i] * v0[i];
+          for (int i = 0; i < kBW; ++i) sumsq += v0[i] * v0[i];
         }
       }
     } else if constexpr (KIND == EPI_OUT) {
@@ -213,17 +215,17 @@ __device__ __noinline__ float tc_epilogue_blocks(const Problem& P, int tn, uint3
     } else if constexpr (KIND == EPI_NS_GRAM) {
       const float s2 = scale * scale;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v0[i] *= s2;
+      for (int i = 0; i < kBW; ++i) v0[i] *= s2;
       store_rows<__nv_bfloat16>(v0, stage, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
                                 rows_valid, lane);
     } else if constexpr (KIND == EPI_NS_POLY) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v0[i] = e.b * x[i] + e.c * v0[i];
+      for (int i = 0; i < kBW; ++i) v0[i] = e.b * x[i] + e.c * v0[i];
       store_rows<__nv_bfloat16>(v0, stage, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
                                 rows_valid, lane);
     } else if constexpr (KIND == EPI_NS_STEP) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v0[i] = scale * (e.a * x[i] + v0[i]);
+      for (int i = 0; i < kBW; ++i) v0[i] = scale * (e.a * x[i] + v0[i]);
       if (e.out[1])
         store_rows<float>(v0, stage, static_cast<float*>(e.out[1]) + off, e.out_ld, rows_valid,
                           lane);

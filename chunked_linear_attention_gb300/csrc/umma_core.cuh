@@ -18,7 +18,7 @@ constexpr int kATileBytes = kBM * kBK * 2;   // 16 KB
 constexpr int kMaxStages = 8;
 constexpr int kCtrlBytes = 3072;             // barriers, TMEM slot, problem descriptors
 constexpr int kProbOffset = 256;             // problem descriptors inside the control region
-constexpr int kEpiWarps = 4;            // one warp per TMEM lane quarter
+constexpr int kEpiWarps = 8;            // two warps per TMEM lane quarter (column halves)
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 
 struct TileCoord {
@@ -139,7 +139,7 @@ __device__ __forceinline__ void issue_op(const OpCoords& c, uint8_t* dst, int ks
 // TMA producer (one thread): streams every (group, k-step) of one tile through
 // the ring.  `s`/`ph` are the ring position carried across tiles.  Per-operand
 // coordinates live in scalars (no runtime-indexed local arrays in the loop).
-__device__ __forceinline__ bool produce_tile(const CUtensorMap* maps, const Problem& P,
+static __device__ __noinline__ bool produce_tile(const CUtensorMap* maps, const Problem& P,
                                              const SmemPlan& sp, const TileCoord& tc,
                                              uint8_t* tiles, uint32_t stage_bytes, int nstages,
                                              uint64_t* full, uint64_t* empty, int& s,
@@ -187,7 +187,7 @@ __device__ __forceinline__ void drain_producer(uint64_t* full, int nstages, int 
 // MMA issuer (one thread): accumulates one tile into TMEM at column tmem_acc
 // (accumulator j at tmem_acc + j * bn).  Descriptors are scalars built once
 // per group; no runtime-indexed arrays in the k-step loop.
-__device__ __forceinline__ bool mma_tile(const Problem& P, const SmemPlan& sp,
+static __device__ __noinline__ bool mma_tile(const Problem& P, const SmemPlan& sp,
                                          uint32_t tiles_saddr, uint32_t stage_bytes, int nstages,
                                          uint64_t* full, uint64_t* empty, uint32_t tmem_acc,
                                          int& s, uint32_t& ph, int* status,
