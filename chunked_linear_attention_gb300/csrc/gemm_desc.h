@@ -47,7 +47,7 @@ struct OpDesc {
 
 struct EpiDesc {
   int kind;
-  int pad_;
+  int in_tmem;             // EPI_NS_POLY: G comes from the other TMEM accumulator buffer
   void* out[3];
   long long out_ld;       // elements between output rows
   long long out_z;        // elements between output batches

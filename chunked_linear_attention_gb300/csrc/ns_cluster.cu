@@ -54,6 +54,8 @@ __device__ __forceinline__ void ns_patch(const NsLaunch& L, Problem& P, int whic
     P.a[0].map = in ? NM_X1_A : NM_X0_A;
     P.b[0].map = in ? NM_X1_B : NM_X0_B;
     P.epi.first = t == 0;
+  } else if (which == 1) {   // Bm = b G + c G G, G from the other TMEM buffer
+    P.epi.first = t == 0;
   } else if (which == 2) {   // X' = a X + Bm X
     P.b[0].map = in ? NM_X1_MN : NM_X0_MN;
     P.epi.in0 = L.X[in];
@@ -358,6 +360,7 @@ int launch_ns_cluster(MapCache& cache, const NsArgs& a, int* status, unsigned lo
   L.poly.epi.out[0] = a.Bm;
   L.poly.epi.b = a.ns[1];
   L.poly.epi.c = a.ns[2];
+  L.poly.epi.in_tmem = 1;   // each CTA keeps its Gram tile in TMEM for the next product
   L.step = base(d);
   L.step.a[0] = op(NM_BM_A, 0);
   L.step.b[0] = op(NM_X0_MN, 1);

@@ -126,15 +126,17 @@ __device__ __noinline__ float tc_epilogue_blocks(const Problem& P, int tn, uint3
                                                     float* stage, int lane) {
   const EpiDesc& e = P.epi;
   const int bn = P.bn;
-  constexpr bool kInBf16 = KIND == EPI_NS_POLY || KIND == EPI_NS_STEP;
+  constexpr bool kInBf16 = KIND == EPI_NS_STEP || (KIND == EPI_NS_POLY);
   constexpr bool kInF32 = KIND == EPI_GRAD;   // used only when e.mom is set
   constexpr int kAcc = KIND == EPI_PROJ_K ? 3 : (KIND == EPI_PROJ_Q ? 2 : 1);
   const bool has_mom = kInF32 && e.mom != nullptr;
+  // the polynomial product may take G from the other TMEM accumulator buffer
+  const bool x_tmem = KIND == EPI_NS_POLY && e.in_tmem;
   BlockRegs<__nv_bfloat16> gin16;
   BlockRegs<float> gin32;
   auto prefetch = [&](int c0) {
     const int gcol = tn * bn + c0;
-    if (rows_valid <= 0 || gcol >= P.N) return;
+    if (rows_valid <= 0 || gcol >= P.N || x_tmem) return;
     if constexpr (kInBf16)
       block_load(static_cast<const __nv_bfloat16*>(e.in0) + tile_base + gcol, e.out_ld,
                  rows_valid, gin16, lane);
@@ -154,7 +156,14 @@ __device__ __noinline__ float tc_epilogue_blocks(const Problem& P, int tn, uint3
     const int gcol = tn * bn + c0;
     const bool active = rows_valid > 0 && gcol < P.N;
     if constexpr (kInBf16 || kInF32) {
-      if (active && (kInBf16 || has_mom)) {
+      if (x_tmem) {
+        if constexpr (KIND == EPI_NS_POLY) {
+          tmem_ld16_nowait((tl + c0) ^ 256u, x);
+          tmem_wait_bind(x);
+#pragma unroll
+          for (int i = 0; i < kBW; ++i) x[i] *= scale * scale;
+        }
+      } else if (active && (kInBf16 || has_mom)) {
         if constexpr (kInBf16) block_to_stage(gin16, stage, lane);
         else block_to_stage(gin32, stage, lane);
         __syncwarp();
@@ -262,7 +271,9 @@ __device__ __forceinline__ float tc_epilogue_tile(const Problem& P, int z, int t
   float eta = 0.f, scale = 1.f;
   if (e.kind == EPI_PROJ_K && myrow < P.M)
     eta = e.eta[(long long)zz * e.eta_z + e.eta_row0 + myrow];
-  if ((e.kind == EPI_NS_GRAM || e.kind == EPI_NS_STEP) && e.first) scale = ns_scale(e, zz);
+  if ((e.kind == EPI_NS_GRAM || e.kind == EPI_NS_STEP || (e.kind == EPI_NS_POLY && e.in_tmem)) &&
+      e.first)
+    scale = ns_scale(e, zz);
 
   const bool ok = mbar_wait(accf, accf_parity, status, lim);
   *ok_out = ok;
