@@ -25,24 +25,29 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 bool MapCache::get(const TensorRef& t, int box_rows, CUtensorMap* out) {
   for (const Entry& e : entries_)
-    if (e.ptr == t.ptr && e.rows == t.rows && e.inner == t.inner && e.box_rows == box_rows) {
+    if (e.ptr == t.ptr && e.bf16 == t.bf16 && e.rows == t.rows && e.inner == t.inner &&
+        e.box_rows == box_rows) {
       *out = e.map;
       return true;
     }
   auto fn = encode_fn();
-  if (!fn || !t.bf16) return false;
-  if ((reinterpret_cast<uintptr_t>(t.ptr) & 15) != 0 || (t.inner * 2) % 16 != 0) return false;
+  if (!fn) return false;
+  const int es = t.bf16 ? 2 : 4;
+  if ((reinterpret_cast<uintptr_t>(t.ptr) & 15) != 0 || (t.inner * es) % 16 != 0) return false;
   Entry e;
   e.ptr = t.ptr;
+  e.bf16 = t.bf16;
   e.rows = t.rows;
   e.inner = t.inner;
   e.box_rows = box_rows;
+  // one 128-byte swizzle row across: 64 bf16 or 32 fp32 elements
   cuuint64_t dims[2] = {(cuuint64_t)t.inner, (cuuint64_t)t.rows};
-  cuuint64_t strides[1] = {(cuuint64_t)t.inner * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint64_t strides[1] = {(cuuint64_t)t.inner * es};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(&e.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(t.ptr), dims,
-                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = fn(&e.map, t.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                  2, const_cast<void*>(t.ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
   entries_.push_back(e);
@@ -77,6 +82,10 @@ OpDesc LaunchBuilder::op(const TensorRef& t, int mn_major, int outer_base, int z
   o.ld = t.inner;
   o.z_stride = (long long)z_outer * t.inner;
   if (tc_) {
+    if (!t.bf16) {   // the tensor-core GEMM takes bf16 operands only
+      ok_ = false;
+      return o;
+    }
     const int box = mn_major ? 64 : box_rows;
     int slot = -1;
     for (int i = 0; i < nmaps_; ++i)

@@ -22,6 +22,7 @@ struct TensorRef {
 };
 
 // TMA descriptors encoded during one call, keyed by view and box height.
+// Boxes are one 128-byte swizzle row wide (64 bf16 or 32 fp32 elements).
 class MapCache {
  public:
   bool get(const TensorRef& t, int box_rows, CUtensorMap* out);
@@ -29,6 +30,7 @@ class MapCache {
  private:
   struct Entry {
     const void* ptr;
+    int bf16;
     long long rows;
     int inner;
     int box_rows;

@@ -19,6 +19,7 @@
 // Matrix slots: 0 = W1 [m, d], 1 = W3 [m, d], 2 = W2 [d, m]; every
 // per-matrix buffer is [slot][B*H][rows*cols].
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <vector>
 
@@ -26,11 +27,24 @@
 #include "layer.h"
 #include "exec.h"
 #include "ns_cluster.h"
+#include "ns_panel.h"
 #include "prof.h"
 
 namespace ttt {
 
 namespace {
+
+// Row-panel Newton-Schulz kernel for d % 128 == 0 (d <= 512) unless
+// TTT_NS_PANEL=0; the tile-cluster kernel otherwise.
+bool use_ns_panel(int d) {
+  static int env = -1;
+  if (env < 0) {
+    const char* s = std::getenv("TTT_NS_PANEL");
+    env = (s && s[0] == '0') ? 0 : 1;
+  }
+  return env == 1 && ns_panel_applicable(d);
+}
+
 
 constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -262,7 +276,8 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
       na.ns[0] = D.ns[0];
       na.ns[1] = D.ns[1];
       na.ns[2] = D.ns[2];
-      const int rc = launch_ns_cluster(cache, na, L.status, L.wait_ns, st);
+      int rc = use_ns_panel(d) ? launch_ns_panel(cache, na, L.status, L.wait_ns, st) : 1;
+      if (rc == 1) rc = launch_ns_cluster(cache, na, L.status, L.wait_ns, st);
       if (rc < 0) return rc;
       fused_update = rc == 0;
     }
@@ -389,7 +404,24 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
 bool per_sequence_streams(const LayerDims& D) {
   if (!D.bf16 || D.B * D.H < 2) return false;
   if (D.muon_steps == 0) return true;
-  return D.d == D.m && prepare_ns_cluster(D.d);
+  return D.d == D.m && ((use_ns_panel(D.d) && prepare_ns_panel(D.d)) || prepare_ns_cluster(D.d));
+}
+
+// Number of stream groups the (batch, head) sequences are split into: each
+// group's launches cover a contiguous range of sequences on its own stream.
+// TTT_SEQUENCE_GROUPS (1 .. B*H) overrides the default of one group per
+// sequence; 1 runs every launch batched over all sequences on the caller's
+// stream.
+int sequence_groups(const LayerDims& D) {
+  const int BH = D.B * D.H;
+  if (!per_sequence_streams(D)) return 1;
+  static int env = -2;
+  if (env == -2) {
+    const char* s = std::getenv("TTT_SEQUENCE_GROUPS");
+    env = (s && s[0]) ? std::atoi(s) : -1;
+  }
+  if (env >= 1) return env < BH ? env : BH;
+  return BH;
 }
 
 int enqueue_all(LayerPlan& L, cudaStream_t st) {
@@ -415,10 +447,12 @@ int enqueue_all(LayerPlan& L, cudaStream_t st) {
   }
   MapCache cache;
   std::vector<cudaStream_t> kids;
-  if (per_sequence_streams(D) && stream_pool(BH, &kids)) {
+  const int groups = sequence_groups(D);
+  if (groups > 1 && stream_pool(groups, &kids)) {
     TTT_CK(fork_streams(st, kids));
-    for (int h = 0; h < BH; ++h) {
-      const int rc = enqueue_range(L, cache, h, 1, kids[h]);
+    for (int g = 0; g < groups; ++g) {
+      const int h0 = (int)((long long)BH * g / groups), h1 = (int)((long long)BH * (g + 1) / groups);
+      const int rc = enqueue_range(L, cache, h0, h1 - h0, kids[g]);
       if (rc != 0) return rc;
     }
     TTT_CK(join_streams(st, kids));
@@ -512,7 +546,10 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
   // one-time device setup outside any capture
   if (tc) {
     if (prepare_umma_gemm() != cudaSuccess) return -6;
-    if (muon && d == m) prepare_ns_cluster(d);
+    if (muon && d == m) {
+      if (use_ns_panel(d)) prepare_ns_panel(d);
+      prepare_ns_cluster(d);
+    }
   }
   return run_cached(key, a.stream, [&](cudaStream_t s) { return enqueue_all(L, s); });
 }

@@ -117,13 +117,40 @@ __device__ __forceinline__ void store_rows(const float (&v)[kBW], float* stage, 
   __syncwarp();
 }
 
+// One block of a gradient epilogue: M = beta M + g (momentum present), then
+// the fp32 update source and/or the bf16 Newton-Schulz input with its squared
+// norm.  `x` holds the old momentum when e.mom is set.
+__device__ __forceinline__ float grad_block(const EpiDesc& e, float (&v0)[kBW],
+                                            const float (&x)[kBW], long long off, int rows_valid,
+                                            float* stage, int lane) {
+  float sumsq = 0.f;
+  if (e.mom) {
+#pragma unroll
+    for (int i = 0; i < kBW; ++i) v0[i] = e.a * x[i] + v0[i];
+    store_rows<float>(v0, stage, e.mom + off, e.out_ld, rows_valid, lane);
+  }
+  if (e.out[0])
+    store_rows<float>(v0, stage, static_cast<float*>(e.out[0]) + off, e.out_ld, rows_valid, lane);
+  if (e.out[1]) {
+    store_rows<__nv_bfloat16>(v0, stage, static_cast<__nv_bfloat16*>(e.out[1]) + off, e.out_ld,
+                              rows_valid, lane);
+    if (lane < rows_valid) {
+#pragma unroll
+      for (int i = 0; i < kBW; ++i) sumsq += v0[i] * v0[i];
+    }
+  }
+  return sumsq;
+}
+
 // Blocks of one tile for one epilogue kind (the kind is uniform per tile, so
 // each kind is its own non-inlined loop and keeps only the registers it needs).
 template <int KIND>
 __device__ __noinline__ float tc_epilogue_blocks(const Problem& P, int tn, uint32_t tl,
                                                     int c_begin, int c_end, long long tile_base,
                                                     int rows_valid, float eta, float scale,
-                                                    float* stage, int lane) {
+                                                    float* stage, int lane, uint64_t* accf,
+                                                    uint32_t accf_parity, int* status,
+                                                    unsigned long long lim, bool* ok_out) {
   const EpiDesc& e = P.epi;
   const int bn = P.bn;
   constexpr bool kInBf16 = KIND == EPI_NS_STEP || (KIND == EPI_NS_POLY);
@@ -143,8 +170,14 @@ __device__ __noinline__ float tc_epilogue_blocks(const Problem& P, int tn, uint3
     if constexpr (kInF32)
       if (has_mom) block_load(e.mom + tile_base + gcol, e.out_ld, rows_valid, gin32, lane);
   };
+  // the first input block is requested before the accumulator is ready, then
+  // inputs run one block ahead
   prefetch(c_begin);
+  const bool ok = mbar_wait(accf, accf_parity, status, lim);
+  *ok_out = ok;
+  tc_fence_after();
   float sumsq = 0.f;
+  if (!ok) return sumsq;
   for (int c0 = c_begin; c0 < c_end; c0 += kBW) {
     float v0[kBW];
     float v1[kAcc > 1 ? kBW : 1];
@@ -202,22 +235,7 @@ __device__ __noinline__ float tc_epilogue_blocks(const Problem& P, int tn, uint3
       store_rows<__nv_bfloat16>(v2, stage, static_cast<__nv_bfloat16*>(e.out[2]) + off, e.out_ld,
                                 rows_valid, lane);
     } else if constexpr (KIND == EPI_GRAD) {
-      if (has_mom) {
-#pragma unroll
-        for (int i = 0; i < kBW; ++i) v0[i] = e.a * x[i] + v0[i];
-        store_rows<float>(v0, stage, e.mom + off, e.out_ld, rows_valid, lane);
-      }
-      if (e.out[0])
-        store_rows<float>(v0, stage, static_cast<float*>(e.out[0]) + off, e.out_ld, rows_valid,
-                          lane);
-      if (e.out[1]) {
-        store_rows<__nv_bfloat16>(v0, stage, static_cast<__nv_bfloat16*>(e.out[1]) + off,
-                                  e.out_ld, rows_valid, lane);
-        if (lane < rows_valid) {
-#pragma unroll
-          for (int i = 0; i < kBW; ++i) sumsq += v0[i] * v0[i];
-        }
-      }
+      sumsq += grad_block(e, v0, x, off, rows_valid, stage, lane);
     } else if constexpr (KIND == EPI_OUT) {
       store_rows<__nv_bfloat16>(v0, stage, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
                                 rows_valid, lane);
@@ -275,36 +293,34 @@ __device__ __forceinline__ float tc_epilogue_tile(const Problem& P, int z, int t
       e.first)
     scale = ns_scale(e, zz);
 
-  const bool ok = mbar_wait(accf, accf_parity, status, lim);
-  *ok_out = ok;
-  tc_fence_after();
-  if (!ok) return 0.f;
   switch (e.kind) {
     case EPI_STORE_F32:
       return tc_epilogue_blocks<EPI_STORE_F32>(P, tn, tl, c_begin, c_end, tile_base, rows_valid,
-                                               eta, scale, stage, lane);
+                                               eta, scale, stage, lane, accf, accf_parity, status, lim, ok_out);
     case EPI_PROJ_Q:
       return tc_epilogue_blocks<EPI_PROJ_Q>(P, tn, tl, c_begin, c_end, tile_base, rows_valid, eta,
-                                            scale, stage, lane);
+                                            scale, stage, lane, accf, accf_parity, status, lim, ok_out);
     case EPI_PROJ_K:
       return tc_epilogue_blocks<EPI_PROJ_K>(P, tn, tl, c_begin, c_end, tile_base, rows_valid, eta,
-                                            scale, stage, lane);
+                                            scale, stage, lane, accf, accf_parity, status, lim, ok_out);
     case EPI_GRAD:
       return tc_epilogue_blocks<EPI_GRAD>(P, tn, tl, c_begin, c_end, tile_base, rows_valid, eta,
-                                          scale, stage, lane);
+                                          scale, stage, lane, accf, accf_parity, status, lim, ok_out);
     case EPI_OUT:
       return tc_epilogue_blocks<EPI_OUT>(P, tn, tl, c_begin, c_end, tile_base, rows_valid, eta,
-                                         scale, stage, lane);
+                                         scale, stage, lane, accf, accf_parity, status, lim, ok_out);
     case EPI_NS_GRAM:
       return tc_epilogue_blocks<EPI_NS_GRAM>(P, tn, tl, c_begin, c_end, tile_base, rows_valid,
-                                             eta, scale, stage, lane);
+                                             eta, scale, stage, lane, accf, accf_parity, status, lim, ok_out);
     case EPI_NS_POLY:
       return tc_epilogue_blocks<EPI_NS_POLY>(P, tn, tl, c_begin, c_end, tile_base, rows_valid,
-                                             eta, scale, stage, lane);
+                                             eta, scale, stage, lane, accf, accf_parity, status, lim, ok_out);
     case EPI_NS_STEP:
       return tc_epilogue_blocks<EPI_NS_STEP>(P, tn, tl, c_begin, c_end, tile_base, rows_valid,
-                                             eta, scale, stage, lane);
+                                             eta, scale, stage, lane, accf, accf_parity, status, lim, ok_out);
     default:
+      *ok_out = mbar_wait(accf, accf_parity, status, lim);
+      tc_fence_after();
       return 0.f;
   }
 }

@@ -123,6 +123,15 @@ BF16_CASES = [
     dict(mode=W.STRIDED, chunk=128, N=1024, d_h=128, m_h=256,
          update_chunks=(1, 0, 1, 1, 0, 0, 0, 0)),
     dict(mode=W.APPLY_THEN_UPDATE, chunk=128, N=512, d_h=64, m_h=64, l2norm=False),
+    # square orders that are multiples of 128: the row-panel Newton-Schulz kernel
+    # with clusters of 2, 3 and 4 CTAs, one step without normalisation
+    dict(mode=W.APPLY_THEN_UPDATE, chunk=256, N=768, d_h=256, m_h=256, muon_steps=3,
+         momentum_beta=0.9),
+    dict(mode=W.APPLY_THEN_UPDATE, chunk=384, N=768, d_h=384, m_h=384, muon_steps=5,
+         momentum_beta=0.9, l2_normed_k=True),
+    dict(mode=W.BLOCK_CAUSAL, chunk=256, N=512, d_h=512, m_h=512, muon_steps=2),
+    dict(mode=W.APPLY_THEN_UPDATE, chunk=128, N=384, d_h=384, m_h=384, muon_steps=1,
+         l2norm=False),
 ]
 
 
