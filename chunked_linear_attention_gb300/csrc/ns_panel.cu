@@ -21,7 +21,7 @@
 // costs two cluster barriers.  The last step's epilogue applies the update
 // and row normalisation directly from TMEM.
 //
-// Warp roles (320 threads): warp 0 lane 0 issues the TMA loads, warp 1 lane 0
+// Warp roles (320 threads): warp 0 lanes 0-1 issue the TMA loads, warp 1 lane 0
 // the tcgen05 MMAs, warps 2..9 drain TMEM (warp w reads lanes 32 (w % 4) ..,
 // column half (w - 2) / 4).  Every mbarrier wait is bounded and reports
 // TTT_ERR_TIMEOUT; every thread reaches every cluster barrier.
@@ -42,6 +42,7 @@ constexpr int kPanelThreads = 320;
 constexpr int kPanelCtrl = 2048;        // barriers, TMEM slot, row sums
 constexpr int kPanelMaxStages = 8;
 constexpr int kPanelChunk = 128 * 64 * 2;   // one 64-column chunk of a 128-row panel
+constexpr int kProdLanes = 2;               // TMA-issuing lanes of warp 0
 
 enum PanelMap : int {
   PM_X0 = 0, PM_X1, PM_G,        // 64 x 64 boxes: B-operand shares
@@ -263,14 +264,16 @@ __global__ void __launch_bounds__(kPanelThreads, 1)
     const int p_begin = (iv & 1) ? 3 * t + 1 : 3 * t;
     const int p_end = (iv & 1) ? 3 * t + 3 : 3 * t + 1;
     if (warp == 0) {
-      if (lane == 0 && ok) {
+      // kProdLanes lanes share the ring entries round robin: one thread cannot
+      // issue the multicast boxes fast enough to keep the tensor cores busy
+      if (lane < kProdLanes && ok) {
         fence_proxy_async_global();
-        if (iv == 0) {
+        if (iv == 0 && lane == 0) {
           mbar_arrive_expect_tx(abar, (uint32_t)(nk * kPanelChunk));
           for (int c = 0; c < nk; ++c)
             tma_load_2d(apanel + c * kPanelChunk, &L.maps[PM_X0_P], c * 64, prow, abar);
         }
-        if (iv == nint - 1) {   // the final update reads this CTA's fp32 W rows
+        if (iv == nint - 1 && lane == 0) {   // the final update reads this CTA's fp32 W rows
           const int slot = z / L.BH, bh = z % L.BH;
           const char* wp = reinterpret_cast<const char*>(
               L.W[slot] + ((long long)bh * d + rank * 128) * d);
@@ -283,17 +286,19 @@ __global__ void __launch_bounds__(kPanelThreads, 1)
           const CUtensorMap* map = kind == 1 ? &L.maps[PM_G] : &L.maps[(tp & 1) ? PM_X1 : PM_X0];
           for (int h = 0; h < 2 && ok; ++h) {
             for (int ks = 0; ks < nk; ++ks) {
-              if (!mbar_wait(&empty[s_prod], ph_prod ^ 1, L.status, lim)) {
-                ok = false;
-                break;
+              if ((issued % kProdLanes) == lane) {
+                if (!mbar_wait(&empty[s_prod], ph_prod ^ 1, L.status, lim)) {
+                  ok = false;
+                  break;
+                }
+                mbar_arrive_expect_tx(&full[s_prod], stage_bytes);
+                uint8_t* dst = ring + s_prod * stage_bytes + rank * 8192;
+                if (kind == 2)   // X as MN-major B: K = rows of X, N = its columns
+                  tma_load_2d_mc(dst, map, h * half + rank * 64, mrow + ks * 64, &full[s_prod], mask);
+                else             // rows of X or G as K-major B
+                  tma_load_2d_mc(dst, map, ks * 64, mrow + h * half + rank * 64, &full[s_prod], mask);
               }
-              mbar_arrive_expect_tx(&full[s_prod], stage_bytes);
-              uint8_t* dst = ring + s_prod * stage_bytes + rank * 8192;
-              if (kind == 2)   // X as MN-major B: K = rows of X, N = its columns
-                tma_load_2d_mc(dst, map, h * half + rank * 64, mrow + ks * 64, &full[s_prod], mask);
-              else             // rows of X or G as K-major B
-                tma_load_2d_mc(dst, map, ks * 64, mrow + h * half + rank * 64, &full[s_prod], mask);
-              ++issued;
+              ++issued;   // every producer lane walks every entry
               if (++s_prod == nstages) {
                 s_prod = 0;
                 ph_prod ^= 1;

@@ -1,17 +1,18 @@
 // Tensor-core epilogue: drains one tile's TMEM accumulators and applies the
 // fused epilogue of epilogue.cuh, with memory traffic shaped for the GPU:
 //
-//   * each epilogue warp owns 32 rows (its TMEM lane quarter) and the tile's
-//     columns, processed in blocks of kBW columns;
+//   * each epilogue warp owns 32 rows (its TMEM lane quarter) and about a
+//     third of the tile's columns (three warps per lane quarter keep enough
+//     loads and stores in flight), processed in blocks of 16 columns;
 //   * per-row scalars (eta, the Newton-Schulz scale) are read once per tile,
-//     before waiting for the accumulator;
-//   * input tiles (momentum, Newton-Schulz iterates) are fetched with
-//     coalesced 16-byte loads one block ahead, then transposed through a
-//     padded per-warp staging buffer in shared memory;
-//   * outputs go back through the same buffer and leave as coalesced 16-byte
-//     stores that cover whole 64/128-byte row segments.
-// The staging buffer holds 32 rows x (kBW + 1) floats (the pad spreads both
-// the row-wise and the chunk-wise accesses over the banks).
+//     and the first input block is requested, before waiting for the
+//     accumulator;
+//   * rows move between a lane's registers and coalesced global accesses
+//     through a 2 KB per-warp staging block in shared memory, in 16-byte
+//     units with an XOR swizzle that keeps both the row-wise and the
+//     coalesced passes free of bank conflicts: a lane packs its row segment
+//     (BW values) into 16-byte units, then the warp stores whole row
+//     segments of consecutive rows with 16-byte vector stores.
 #pragma once
 
 #include "common.cuh"
@@ -20,123 +21,138 @@
 
 namespace ttt {
 
-constexpr int kBW = 16;                               // columns per epilogue block
-constexpr int kStageStride = kBW + 1;                 // floats per staged row (padded)
-constexpr int kStageFloats = 32 * kStageStride;       // per warp
-// all epilogue warps' staging buffers, rounded up to keep the stage ring 1 KB aligned
-constexpr int kStagingBytes = (kEpiWarps * kStageFloats * 4 + 1023) / 1024 * 1024;
+constexpr int kStageBytesPerWarp = 2048;                 // 32 rows x 64 bytes
+constexpr int kStageFloats = kStageBytesPerWarp / 4;     // per-warp stride in floats
+constexpr int kStagingBytes = kEpiWarps * kStageBytesPerWarp;
+static_assert(kStagingBytes % 1024 == 0, "keeps the stage ring 1 KB aligned");
 
-// 32 x kBW block of T starting at `base` of a row-major matrix with leading
-// dimension ld; one warp, coalesced 16-byte accesses.
-template <typename T>
-struct BlockRegs {
-  static constexpr int kCPR = kBW * (int)sizeof(T) / 16;   // 16-byte chunks per row
-  static constexpr int kRPI = 32 / kCPR;                    // rows per warp instruction
-  uint4 r[32 / kRPI];
+// Byte offset of 16-byte unit u of row r in a 32-row staging block whose rows
+// are RB bytes (RB = 32 or 64).  The XOR spreads the 8 lanes of one shared
+// memory phase over all banks, for the row-wise and the coalesced pattern.
+template <int RB>
+__device__ __forceinline__ uint32_t stage_off(int r, int u) {
+  static_assert(RB == 32 || RB == 64, "row bytes");
+  if constexpr (RB == 32) return (uint32_t)(r * 32 + ((u ^ ((r >> 2) & 1)) << 4));
+  else return (uint32_t)(r * 64 + ((u ^ ((r >> 1) & 3)) << 4));
+}
+
+template <int BW>
+__device__ __forceinline__ void tmem_load_block(uint32_t taddr, float (&v)[BW]) {
+  static_assert(BW == 16 || BW == 32, "block width");
+  if constexpr (BW == 16) tmem_ld16_nowait(taddr, v);
+  else tmem_ld32(taddr, v);
+}
+template <int BW>
+__device__ __forceinline__ void tmem_wait_block(float (&v)[BW]) {
+  if constexpr (BW == 16) tmem_wait_bind(v);
+  else tmem_wait32(v);
+}
+
+// 16-byte units of a 32-row block of T, BW columns, held as coalesced
+// registers: unit i of this lane is unit (i * 32 + lane) of the block.
+template <typename T, int BW>
+struct BlockIn {
+  static constexpr int kRB = BW * (int)sizeof(T);   // bytes per row
+  static constexpr int kU = kRB / 16;               // units per row
+  uint4 w[kU];
 };
 
-template <typename T>
-__device__ __forceinline__ void block_load(const T* base, long long ld, int rows_valid,
-                                           BlockRegs<T>& g, int lane) {
-  constexpr int kCPR = BlockRegs<T>::kCPR;
-  constexpr int kRPI = BlockRegs<T>::kRPI;
+// Coalesced global -> registers (rows >= rows_valid read as zero).
+template <typename T, int BW>
+__device__ __forceinline__ void block_fetch(const T* base, long long ld, int rows_valid,
+                                            BlockIn<T, BW>& g, int lane) {
+  constexpr int U = BlockIn<T, BW>::kU;
 #pragma unroll
-  for (int i = 0; i < 32 / kRPI; ++i) {
-    const int r = i * kRPI + lane / kCPR;
-    const int ch = lane % kCPR;
-    if (r < rows_valid)
-      g.r[i] = *reinterpret_cast<const uint4*>(base + (long long)r * ld + ch * (16 / sizeof(T)));
-    else
-      g.r[i] = make_uint4(0, 0, 0, 0);
+  for (int i = 0; i < U; ++i) {
+    const int idx = i * 32 + lane, r = idx / U, u = idx % U;
+    g.w[i] = r < rows_valid ? *reinterpret_cast<const uint4*>(
+                                  reinterpret_cast<const char*>(base + (long long)r * ld) + u * 16)
+                            : make_uint4(0, 0, 0, 0);
   }
 }
 
-// Coalesced registers -> staging (as fp32).
-template <typename T>
-__device__ __forceinline__ void block_to_stage(const BlockRegs<T>& g, float* stage, int lane) {
-  constexpr int kCPR = BlockRegs<T>::kCPR;
-  constexpr int kRPI = BlockRegs<T>::kRPI;
-  constexpr int kEPC = 16 / sizeof(T);  // elements per chunk
+// Registers -> staging -> this lane's row (as fp32).
+template <typename T, int BW>
+__device__ __forceinline__ void block_to_row(const BlockIn<T, BW>& g, uint32_t st, float (&x)[BW],
+                                             int lane) {
+  constexpr int RB = BlockIn<T, BW>::kRB, U = BlockIn<T, BW>::kU;
 #pragma unroll
-  for (int i = 0; i < 32 / kRPI; ++i) {
-    const int r = i * kRPI + lane / kCPR;
-    const int c = (lane % kCPR) * kEPC;
-    float* dst = stage + r * kStageStride + c;
-    const uint4 v = g.r[i];
+  for (int i = 0; i < U; ++i) {
+    const int idx = i * 32 + lane;
+    sts128(st + stage_off<RB>(idx / U, idx % U), g.w[i]);
+  }
+  __syncwarp();
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const uint4 w = lds128(st + stage_off<RB>(lane, u));
     if constexpr (sizeof(T) == 2) {
-      dst[0] = bf16lo(v.x); dst[1] = bf16hi(v.x); dst[2] = bf16lo(v.y); dst[3] = bf16hi(v.y);
-      dst[4] = bf16lo(v.z); dst[5] = bf16hi(v.z); dst[6] = bf16lo(v.w); dst[7] = bf16hi(v.w);
+      x[8 * u + 0] = bf16lo(w.x); x[8 * u + 1] = bf16hi(w.x);
+      x[8 * u + 2] = bf16lo(w.y); x[8 * u + 3] = bf16hi(w.y);
+      x[8 * u + 4] = bf16lo(w.z); x[8 * u + 5] = bf16hi(w.z);
+      x[8 * u + 6] = bf16lo(w.w); x[8 * u + 7] = bf16hi(w.w);
     } else {
-      dst[0] = __uint_as_float(v.x); dst[1] = __uint_as_float(v.y);
-      dst[2] = __uint_as_float(v.z); dst[3] = __uint_as_float(v.w);
+      x[4 * u + 0] = __uint_as_float(w.x); x[4 * u + 1] = __uint_as_float(w.y);
+      x[4 * u + 2] = __uint_as_float(w.z); x[4 * u + 3] = __uint_as_float(w.w);
     }
   }
+  __syncwarp();
 }
 
-// Staging -> global, coalesced, converting to T.
-template <typename T>
-__device__ __forceinline__ void stage_to_global(const float* stage, T* base, long long ld,
-                                                int rows_valid, int lane) {
-  constexpr int kCPR = BlockRegs<T>::kCPR;
-  constexpr int kRPI = BlockRegs<T>::kRPI;
-  constexpr int kEPC = 16 / sizeof(T);
-#pragma unroll
-  for (int i = 0; i < 32 / kRPI; ++i) {
-    const int r = i * kRPI + lane / kCPR;
-    const int c = (lane % kCPR) * kEPC;
-    const float* s = stage + r * kStageStride + c;
-    uint4 v;
-    if constexpr (sizeof(T) == 2) {
-      v = make_uint4(pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]), pack_bf16x2(s[4], s[5]),
-                     pack_bf16x2(s[6], s[7]));
-    } else {
-      v = make_uint4(__float_as_uint(s[0]), __float_as_uint(s[1]), __float_as_uint(s[2]),
-                     __float_as_uint(s[3]));
-    }
-    if (r < rows_valid) *reinterpret_cast<uint4*>(base + (long long)r * ld + c) = v;
-  }
-}
-
-// This thread's row of kBW values: registers -> staging row / staging row -> registers.
-__device__ __forceinline__ void row_to_stage(const float (&v)[kBW], float* stage, int lane) {
-#pragma unroll
-  for (int j = 0; j < kBW; ++j) stage[lane * kStageStride + j] = v[j];
-}
-__device__ __forceinline__ void stage_to_row(const float* stage, float (&v)[kBW], int lane) {
-#pragma unroll
-  for (int j = 0; j < kBW; ++j) v[j] = stage[lane * kStageStride + j];
-}
-
-// Writes a row-held block through the staging buffer to global memory.
-template <typename T>
-__device__ __forceinline__ void store_rows(const float (&v)[kBW], float* stage, T* base, long long ld,
+// This lane's row (BW values) -> staging -> coalesced global stores as T.
+template <typename T, int BW>
+__device__ __forceinline__ void store_rows(const float (&v)[BW], uint32_t st, T* base, long long ld,
                                            int rows_valid, int lane) {
-  row_to_stage(v, stage, lane);
+  constexpr int RB = BlockIn<T, BW>::kRB, U = BlockIn<T, BW>::kU;
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    uint4 w;
+    if constexpr (sizeof(T) == 2) {
+      w = make_uint4(pack_bf16x2(v[8 * u], v[8 * u + 1]), pack_bf16x2(v[8 * u + 2], v[8 * u + 3]),
+                     pack_bf16x2(v[8 * u + 4], v[8 * u + 5]),
+                     pack_bf16x2(v[8 * u + 6], v[8 * u + 7]));
+    } else {
+      w = make_uint4(__float_as_uint(v[4 * u]), __float_as_uint(v[4 * u + 1]),
+                     __float_as_uint(v[4 * u + 2]), __float_as_uint(v[4 * u + 3]));
+    }
+    sts128(st + stage_off<RB>(lane, u), w);
+  }
   __syncwarp();
-  stage_to_global<T>(stage, base, ld, rows_valid, lane);
+#pragma unroll
+  for (int i = 0; i < U; ++i) {
+    const int idx = i * 32 + lane, r = idx / U, u = idx % U;
+    const uint4 w = lds128(st + stage_off<RB>(r, u));
+    if (r < rows_valid)
+      *reinterpret_cast<uint4*>(reinterpret_cast<char*>(base + (long long)r * ld) + u * 16) = w;
+  }
   __syncwarp();
+}
+
+// Columns per block for each epilogue kind: 16 where three accumulators or
+// fp32 rows must fit the registers and the 2 KB staging block.
+template <int KIND>
+constexpr int epi_block_width() {
+  return (kEpiWarps == 8 && (KIND == EPI_PROJ_Q || KIND == EPI_OUT)) ? 32 : 16;
 }
 
 // One block of a gradient epilogue: M = beta M + g (momentum present), then
 // the fp32 update source and/or the bf16 Newton-Schulz input with its squared
 // norm.  `x` holds the old momentum when e.mom is set.
-__device__ __forceinline__ float grad_block(const EpiDesc& e, float (&v0)[kBW],
-                                            const float (&x)[kBW], long long off, int rows_valid,
-                                            float* stage, int lane) {
+__device__ __forceinline__ float grad_block(const EpiDesc& e, float (&v0)[16], const float (&x)[16],
+                                            long long off, int rows_valid, uint32_t st, int lane) {
   float sumsq = 0.f;
   if (e.mom) {
 #pragma unroll
-    for (int i = 0; i < kBW; ++i) v0[i] = e.a * x[i] + v0[i];
-    store_rows<float>(v0, stage, e.mom + off, e.out_ld, rows_valid, lane);
+    for (int i = 0; i < 16; ++i) v0[i] = e.a * x[i] + v0[i];
+    store_rows<float, 16>(v0, st, e.mom + off, e.out_ld, rows_valid, lane);
   }
   if (e.out[0])
-    store_rows<float>(v0, stage, static_cast<float*>(e.out[0]) + off, e.out_ld, rows_valid, lane);
+    store_rows<float, 16>(v0, st, static_cast<float*>(e.out[0]) + off, e.out_ld, rows_valid, lane);
   if (e.out[1]) {
-    store_rows<__nv_bfloat16>(v0, stage, static_cast<__nv_bfloat16*>(e.out[1]) + off, e.out_ld,
-                              rows_valid, lane);
+    store_rows<__nv_bfloat16, 16>(v0, st, static_cast<__nv_bfloat16*>(e.out[1]) + off, e.out_ld,
+                                  rows_valid, lane);
     if (lane < rows_valid) {
 #pragma unroll
-      for (int i = 0; i < kBW; ++i) sumsq += v0[i] * v0[i];
+      for (int i = 0; i < 16; ++i) sumsq += v0[i] * v0[i];
     }
   }
   return sumsq;
@@ -144,6 +160,7 @@ __device__ __forceinline__ float grad_block(const EpiDesc& e, float (&v0)[kBW],
 
 // Blocks of one tile for one epilogue kind (the kind is uniform per tile, so
 // each kind is its own non-inlined loop and keeps only the registers it needs).
+// Waits (bounded) for the accumulator after requesting the first input block.
 template <int KIND>
 __device__ __noinline__ float tc_epilogue_blocks(const Problem& P, int tn, uint32_t tl,
                                                     int c_begin, int c_end, long long tile_base,
@@ -151,24 +168,26 @@ __device__ __noinline__ float tc_epilogue_blocks(const Problem& P, int tn, uint3
                                                     float* stage, int lane, uint64_t* accf,
                                                     uint32_t accf_parity, int* status,
                                                     unsigned long long lim, bool* ok_out) {
+  constexpr int BW = epi_block_width<KIND>();
   const EpiDesc& e = P.epi;
   const int bn = P.bn;
-  constexpr bool kInBf16 = KIND == EPI_NS_STEP || (KIND == EPI_NS_POLY);
+  const uint32_t st = smem_u32(stage);
+  constexpr bool kInBf16 = KIND == EPI_NS_STEP || KIND == EPI_NS_POLY;
   constexpr bool kInF32 = KIND == EPI_GRAD;   // used only when e.mom is set
   constexpr int kAcc = KIND == EPI_PROJ_K ? 3 : (KIND == EPI_PROJ_Q ? 2 : 1);
   const bool has_mom = kInF32 && e.mom != nullptr;
   // the polynomial product may take G from the other TMEM accumulator buffer
   const bool x_tmem = KIND == EPI_NS_POLY && e.in_tmem;
-  BlockRegs<__nv_bfloat16> gin16;
-  BlockRegs<float> gin32;
+  BlockIn<__nv_bfloat16, BW> gin16;
+  BlockIn<float, BW> gin32;
   auto prefetch = [&](int c0) {
     const int gcol = tn * bn + c0;
     if (rows_valid <= 0 || gcol >= P.N || x_tmem) return;
     if constexpr (kInBf16)
-      block_load(static_cast<const __nv_bfloat16*>(e.in0) + tile_base + gcol, e.out_ld,
-                 rows_valid, gin16, lane);
+      block_fetch(static_cast<const __nv_bfloat16*>(e.in0) + tile_base + gcol, e.out_ld,
+                  rows_valid, gin16, lane);
     if constexpr (kInF32)
-      if (has_mom) block_load(e.mom + tile_base + gcol, e.out_ld, rows_valid, gin32, lane);
+      if (has_mom) block_fetch(e.mom + tile_base + gcol, e.out_ld, rows_valid, gin32, lane);
   };
   // the first input block is requested before the accumulator is ready, then
   // inputs run one block ahead
@@ -178,48 +197,46 @@ __device__ __noinline__ float tc_epilogue_blocks(const Problem& P, int tn, uint3
   tc_fence_after();
   float sumsq = 0.f;
   if (!ok) return sumsq;
-  for (int c0 = c_begin; c0 < c_end; c0 += kBW) {
-    float v0[kBW];
-    float v1[kAcc > 1 ? kBW : 1];
-    float v2[kAcc > 2 ? kBW : 1];
-    float x[(kInBf16 || kInF32) ? kBW : 1];
-    tmem_ld16_nowait(tl + c0, v0);
-    if constexpr (kAcc > 1) tmem_ld16_nowait(tl + bn + c0, v1);
-    if constexpr (kAcc > 2) tmem_ld16_nowait(tl + 2 * bn + c0, v2);
+  for (int c0 = c_begin; c0 < c_end; c0 += BW) {
+    float v0[BW];
+    float v1[kAcc > 1 ? BW : 1];
+    float v2[kAcc > 2 ? BW : 1];
+    float x[(kInBf16 || kInF32) ? BW : 1];
+    tmem_load_block<BW>(tl + c0, v0);
+    if constexpr (kAcc > 1) tmem_load_block<BW>(tl + bn + c0, v1);
+    if constexpr (kAcc > 2) tmem_load_block<BW>(tl + 2 * bn + c0, v2);
     const int gcol = tn * bn + c0;
     const bool active = rows_valid > 0 && gcol < P.N;
     if constexpr (kInBf16 || kInF32) {
       if (x_tmem) {
         if constexpr (KIND == EPI_NS_POLY) {
-          tmem_ld16_nowait((tl + c0) ^ 256u, x);
-          tmem_wait_bind(x);
+          tmem_load_block<BW>((tl + c0) ^ 256u, x);
+          tmem_wait_block<BW>(x);
 #pragma unroll
-          for (int i = 0; i < kBW; ++i) x[i] *= scale * scale;
+          for (int i = 0; i < BW; ++i) x[i] *= scale * scale;
         }
       } else if (active && (kInBf16 || has_mom)) {
-        if constexpr (kInBf16) block_to_stage(gin16, stage, lane);
-        else block_to_stage(gin32, stage, lane);
-        __syncwarp();
-        stage_to_row(stage, x, lane);
-        __syncwarp();
+        if constexpr (kInBf16) block_to_row(gin16, st, x, lane);
+        else block_to_row(gin32, st, x, lane);
       }
     }
-    if (c0 + kBW < c_end) prefetch(c0 + kBW);
-    tmem_wait_bind(v0);
-    if constexpr (kAcc > 1) tmem_wait_bind(v1);
-    if constexpr (kAcc > 2) tmem_wait_bind(v2);
+    if (c0 + BW < c_end) prefetch(c0 + BW);
+    tmem_wait_block<BW>(v0);
+    if constexpr (kAcc > 1) tmem_wait_block<BW>(v1);
+    if constexpr (kAcc > 2) tmem_wait_block<BW>(v2);
     if (!active) continue;
     const long long off = tile_base + gcol;
     if constexpr (KIND == EPI_STORE_F32) {
-      store_rows<float>(v0, stage, static_cast<float*>(e.out[0]) + off, e.out_ld, rows_valid, lane);
+      store_rows<float, BW>(v0, st, static_cast<float*>(e.out[0]) + off, e.out_ld, rows_valid,
+                            lane);
     } else if constexpr (KIND == EPI_PROJ_Q) {
 #pragma unroll
-      for (int i = 0; i < kBW; ++i) v0[i] = v0[i] * sigmoid_f(v0[i]) * v1[i];
-      store_rows<__nv_bfloat16>(v0, stage, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
-                                rows_valid, lane);
+      for (int i = 0; i < BW; ++i) v0[i] = v0[i] * sigmoid_f(v0[i]) * v1[i];
+      store_rows<__nv_bfloat16, BW>(v0, st, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
+                                    rows_valid, lane);
     } else if constexpr (KIND == EPI_PROJ_K) {
 #pragma unroll
-      for (int i = 0; i < kBW; ++i) {
+      for (int i = 0; i < BW; ++i) {
         const float h1 = v0[i], h3 = v1[i];
         const float s = sigmoid_f(h1);
         const float sl = h1 * s;
@@ -228,46 +245,46 @@ __device__ __noinline__ float tc_epilogue_blocks(const Problem& P, int tn, uint3
         v1[i] = dA * sl;                                   // dH3
         v2[i] = -eta * sl * h3;                            // P
       }
-      store_rows<__nv_bfloat16>(v0, stage, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
-                                rows_valid, lane);
-      store_rows<__nv_bfloat16>(v1, stage, static_cast<__nv_bfloat16*>(e.out[1]) + off, e.out_ld,
-                                rows_valid, lane);
-      store_rows<__nv_bfloat16>(v2, stage, static_cast<__nv_bfloat16*>(e.out[2]) + off, e.out_ld,
-                                rows_valid, lane);
+      store_rows<__nv_bfloat16, BW>(v0, st, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
+                                    rows_valid, lane);
+      store_rows<__nv_bfloat16, BW>(v1, st, static_cast<__nv_bfloat16*>(e.out[1]) + off, e.out_ld,
+                                    rows_valid, lane);
+      store_rows<__nv_bfloat16, BW>(v2, st, static_cast<__nv_bfloat16*>(e.out[2]) + off, e.out_ld,
+                                    rows_valid, lane);
     } else if constexpr (KIND == EPI_GRAD) {
-      sumsq += grad_block(e, v0, x, off, rows_valid, stage, lane);
+      sumsq += grad_block(e, v0, x, off, rows_valid, st, lane);
     } else if constexpr (KIND == EPI_OUT) {
-      store_rows<__nv_bfloat16>(v0, stage, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
-                                rows_valid, lane);
+      store_rows<__nv_bfloat16, BW>(v0, st, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
+                                    rows_valid, lane);
     } else if constexpr (KIND == EPI_NS_GRAM) {
       const float s2 = scale * scale;
 #pragma unroll
-      for (int i = 0; i < kBW; ++i) v0[i] *= s2;
-      store_rows<__nv_bfloat16>(v0, stage, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
-                                rows_valid, lane);
+      for (int i = 0; i < BW; ++i) v0[i] *= s2;
+      store_rows<__nv_bfloat16, BW>(v0, st, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
+                                    rows_valid, lane);
     } else if constexpr (KIND == EPI_NS_POLY) {
 #pragma unroll
-      for (int i = 0; i < kBW; ++i) v0[i] = e.b * x[i] + e.c * v0[i];
-      store_rows<__nv_bfloat16>(v0, stage, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
-                                rows_valid, lane);
+      for (int i = 0; i < BW; ++i) v0[i] = e.b * x[i] + e.c * v0[i];
+      store_rows<__nv_bfloat16, BW>(v0, st, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
+                                    rows_valid, lane);
     } else if constexpr (KIND == EPI_NS_STEP) {
 #pragma unroll
-      for (int i = 0; i < kBW; ++i) v0[i] = scale * (e.a * x[i] + v0[i]);
+      for (int i = 0; i < BW; ++i) v0[i] = scale * (e.a * x[i] + v0[i]);
       if (e.out[1])
-        store_rows<float>(v0, stage, static_cast<float*>(e.out[1]) + off, e.out_ld, rows_valid,
-                          lane);
+        store_rows<float, BW>(v0, st, static_cast<float*>(e.out[1]) + off, e.out_ld, rows_valid,
+                              lane);
       else
-        store_rows<__nv_bfloat16>(v0, stage, static_cast<__nv_bfloat16*>(e.out[0]) + off,
-                                  e.out_ld, rows_valid, lane);
+        store_rows<__nv_bfloat16, BW>(v0, st, static_cast<__nv_bfloat16*>(e.out[0]) + off,
+                                      e.out_ld, rows_valid, lane);
     }
   }
   return sumsq;
 }
 
 // Epilogue of one tile on the tensor-core path (bf16 work tensors and I/O).
-// Waits for the accumulator (bounded) after reading the per-row scalars.
-// `warp` is 2..9; `stage` is this warp's staging buffer.  Returns this
-// thread's share of the EPI_GRAD sum of squares.
+// `warp` is 2..9; `stage` is this warp's staging block.  Sets *ok_out to the
+// outcome of the (bounded) accumulator wait.  Returns this thread's share of
+// the EPI_GRAD sum of squares.
 __device__ __forceinline__ float tc_epilogue_tile(const Problem& P, int z, int tm, int tn,
                                                   uint32_t tmem_acc, uint64_t* accf,
                                                   uint32_t accf_parity, int* status,
@@ -284,7 +301,9 @@ __device__ __forceinline__ float tc_epilogue_tile(const Problem& P, int z, int t
   const int zz = e.z_div > 1 ? z / e.z_div : z;
   const long long tile_base = (long long)zz * e.out_z + (e.out_row0 + row0) * e.out_ld;
   const uint32_t tl = tmem_acc + ((uint32_t)(sub * 32) << 16);
-  const int c_begin = slice * (bn / kSplit), c_end = c_begin + bn / kSplit;
+  // the tile's 16-column blocks are shared out in contiguous runs
+  const int nblk = bn / 16;
+  const int c_begin = 16 * (slice * nblk / kSplit), c_end = 16 * ((slice + 1) * nblk / kSplit);
 
   float eta = 0.f, scale = 1.f;
   if (e.kind == EPI_PROJ_K && myrow < P.M)
@@ -293,36 +312,25 @@ __device__ __forceinline__ float tc_epilogue_tile(const Problem& P, int z, int t
       e.first)
     scale = ns_scale(e, zz);
 
+#define TTT_EPI_CASE(K)                                                                        \
+  case K:                                                                                      \
+    return tc_epilogue_blocks<K>(P, tn, tl, c_begin, c_end, tile_base, rows_valid, eta, scale, \
+                                 stage, lane, accf, accf_parity, status, lim, ok_out);
   switch (e.kind) {
-    case EPI_STORE_F32:
-      return tc_epilogue_blocks<EPI_STORE_F32>(P, tn, tl, c_begin, c_end, tile_base, rows_valid,
-                                               eta, scale, stage, lane, accf, accf_parity, status, lim, ok_out);
-    case EPI_PROJ_Q:
-      return tc_epilogue_blocks<EPI_PROJ_Q>(P, tn, tl, c_begin, c_end, tile_base, rows_valid, eta,
-                                            scale, stage, lane, accf, accf_parity, status, lim, ok_out);
-    case EPI_PROJ_K:
-      return tc_epilogue_blocks<EPI_PROJ_K>(P, tn, tl, c_begin, c_end, tile_base, rows_valid, eta,
-                                            scale, stage, lane, accf, accf_parity, status, lim, ok_out);
-    case EPI_GRAD:
-      return tc_epilogue_blocks<EPI_GRAD>(P, tn, tl, c_begin, c_end, tile_base, rows_valid, eta,
-                                          scale, stage, lane, accf, accf_parity, status, lim, ok_out);
-    case EPI_OUT:
-      return tc_epilogue_blocks<EPI_OUT>(P, tn, tl, c_begin, c_end, tile_base, rows_valid, eta,
-                                         scale, stage, lane, accf, accf_parity, status, lim, ok_out);
-    case EPI_NS_GRAM:
-      return tc_epilogue_blocks<EPI_NS_GRAM>(P, tn, tl, c_begin, c_end, tile_base, rows_valid,
-                                             eta, scale, stage, lane, accf, accf_parity, status, lim, ok_out);
-    case EPI_NS_POLY:
-      return tc_epilogue_blocks<EPI_NS_POLY>(P, tn, tl, c_begin, c_end, tile_base, rows_valid,
-                                             eta, scale, stage, lane, accf, accf_parity, status, lim, ok_out);
-    case EPI_NS_STEP:
-      return tc_epilogue_blocks<EPI_NS_STEP>(P, tn, tl, c_begin, c_end, tile_base, rows_valid,
-                                             eta, scale, stage, lane, accf, accf_parity, status, lim, ok_out);
+    TTT_EPI_CASE(EPI_STORE_F32)
+    TTT_EPI_CASE(EPI_PROJ_Q)
+    TTT_EPI_CASE(EPI_PROJ_K)
+    TTT_EPI_CASE(EPI_GRAD)
+    TTT_EPI_CASE(EPI_OUT)
+    TTT_EPI_CASE(EPI_NS_GRAM)
+    TTT_EPI_CASE(EPI_NS_POLY)
+    TTT_EPI_CASE(EPI_NS_STEP)
     default:
       *ok_out = mbar_wait(accf, accf_parity, status, lim);
       tc_fence_after();
       return 0.f;
   }
+#undef TTT_EPI_CASE
 }
 
 }  // namespace ttt

@@ -18,7 +18,7 @@ constexpr int kATileBytes = kBM * kBK * 2;   // 16 KB
 constexpr int kMaxStages = 8;
 constexpr int kCtrlBytes = 3072;             // barriers, TMEM slot, problem descriptors
 constexpr int kProbOffset = 256;             // problem descriptors inside the control region
-constexpr int kEpiWarps = 8;            // two warps per TMEM lane quarter (column halves)
+constexpr int kEpiWarps = 12;           // three warps per TMEM lane quarter (column thirds)
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 
 struct TileCoord {
@@ -146,6 +146,22 @@ static __device__ __noinline__ bool produce_tile(const CUtensorMap* maps, const 
                                              uint32_t& ph, int* status, unsigned long long lim) {
   const int nk = P.K / kBK;
   const uint32_t b_step = P.bn * kBK * 2;
+  if (P.epi.kind == EPI_GRAD && P.epi.mom) {
+    // the epilogue reads this tile's momentum rows: bring them into L2 while
+    // the main loop runs (whole rows, contiguous)
+    const EpiDesc& e = P.epi;
+    const int zz = e.z_div > 1 ? tc.z / e.z_div : tc.z;
+    const int row0 = tc.tm * kBM;
+    const int rows = min(kBM, P.M - row0);
+    if (rows > 0) {
+      const char* base = reinterpret_cast<const char*>(
+          e.mom + (long long)zz * e.out_z + (e.out_row0 + row0) * e.out_ld);
+      const uint32_t bytes = (uint32_t)rows * (uint32_t)e.out_ld * 4u;
+      if ((reinterpret_cast<uintptr_t>(base) & 15) == 0 && (bytes & 15) == 0)
+        for (uint32_t o = 0; o < bytes; o += 16384u)
+          prefetch_l2_bulk(base + o, min(16384u, bytes - o));
+    }
+  }
   for (int g = 0; g < sp.ngroups; ++g) {
     const int j0 = sp.g_first[g], cnt = sp.g_count[g];
     const uint32_t bytes = sp.g_bytes[g];
