@@ -17,6 +17,7 @@ constexpr size_t kMaxGraphs = 8;
 struct DevicePool {
   std::vector<cudaStream_t> streams;
   std::vector<cudaEvent_t> events;
+  std::vector<cudaEvent_t> order_events;
   cudaStream_t capture = nullptr;
 };
 
@@ -70,6 +71,20 @@ bool stream_pool(int n, std::vector<cudaStream_t>* out) {
     p->streams.push_back(s);
   }
   out->assign(p->streams.begin(), p->streams.begin() + n);
+  return true;
+}
+
+bool stagger_events(int n, std::vector<cudaEvent_t>* out) {
+  if (n > kMaxPool) return false;
+  std::lock_guard<std::mutex> lk(g_pool_mu);
+  DevicePool* p = pool_for_current();
+  if (!p) return false;
+  while ((int)p->order_events.size() < n) {
+    cudaEvent_t e;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return false;
+    p->order_events.push_back(e);
+  }
+  out->assign(p->order_events.begin(), p->order_events.begin() + n);
   return true;
 }
 

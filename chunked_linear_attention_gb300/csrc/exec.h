@@ -22,6 +22,10 @@ bool stream_pool(int n, std::vector<cudaStream_t>* out);
 cudaError_t fork_streams(cudaStream_t parent, const std::vector<cudaStream_t>& kids);
 cudaError_t join_streams(cudaStream_t parent, const std::vector<cudaStream_t>& kids);
 
+// `n` events of the current device for ordering between pool streams
+// (separate from the fork/join events).  Returns false on failure.
+bool stagger_events(int n, std::vector<cudaEvent_t>* out);
+
 // Runs `enqueue(stream)` through a cached graph when possible: on the first
 // call with a given key the launch sequence is captured on an internal stream
 // and instantiated; every call then launches the graph on `stream`.  Falls

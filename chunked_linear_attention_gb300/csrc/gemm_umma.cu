@@ -3,10 +3,10 @@
 // epilogues from epilogue.cuh.
 //
 // One CTA per SM (the whole 227 KB of shared memory, all 512 TMEM columns)
-// walks the launch's tiles with a static stride of gridDim.x.  Warp roles
-// (192 threads): warp 0 issues TMA loads into a ring of stages, warp 1 issues
-// tcgen05.mma from one thread, warps 2..5 drain TMEM (tcgen05.ld) and run the
-// epilogue.  When a tile needs at most 256 TMEM columns the accumulator is
+// walks the launch's tiles with a static stride of gridDim.x.  Warp roles:
+// two lanes of warp 0 issue TMA loads into a ring of stages, warp 1 issues
+// tcgen05.mma from one thread, the kEpiWarps warps after them drain TMEM
+// (tcgen05.ld) and run the epilogue.  When a tile needs at most 256 TMEM columns the accumulator is
 // double-buffered, so the epilogue of one tile overlaps the MMAs of the next;
 // the producer always runs ahead into the next tile.  Every wait is bounded
 // and reports TTT_ERR_TIMEOUT into the device status word.
@@ -84,8 +84,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const unsigned long long lim = L.wait_limit_ns;
 
   if (warp == 0) {
-    if (lane == 0) {
-      int s = 0, filled = 0;
+    if (lane < kProdLanes) {
+      int s = 0, filled = 0, e = 0;
       uint32_t ph = 0;
       for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
         const TileCoord tc = decode_tile(probs, nprob, t);
@@ -94,10 +94,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         plan_problem(P, sp);
         filled += sp.ngroups * (P.K / kBK);
         if (!produce_tile(L.maps, P, sp, tc, tiles, stage_bytes, nstages, full, empty, s, ph,
-                          L.status, lim))
+                          lane, kProdLanes, e, L.status, lim))
           break;
       }
-      drain_producer(full, nstages, s, ph, filled, L.status, lim);
+      if (lane == 0) drain_producer(full, nstages, s, ph, filled, L.status, lim);
     }
   } else if (warp == 1) {
     if (lane == 0) {

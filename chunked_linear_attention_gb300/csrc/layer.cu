@@ -150,7 +150,10 @@ struct LayerPlan {
     if ((x) != cudaSuccess) return -6; \
   } while (0)
 
-int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStream_t st) {
+// `after_first`: if set, recorded on `st` once the first step's projection and
+// gradient launches are enqueued (stream groups start staggered on it).
+int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStream_t st,
+                  cudaEvent_t after_first = nullptr) {
   const LayerArgs& a = *L.a;
   const LayerDims& D = *L.D;
   const LayerWs& w = L.w;
@@ -250,6 +253,10 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
     }
     if (!LB.ok()) return -4;
     TTT_CK(LB.launch(st, PT_GRAD));
+    if (after_first) {
+      TTT_CK(cudaEventRecord(after_first, st));
+      after_first = nullptr;
+    }
 
     if (up < 0) continue;
 
@@ -407,11 +414,21 @@ bool per_sequence_streams(const LayerDims& D) {
   return D.d == D.m && ((use_ns_panel(D.d) && prepare_ns_panel(D.d)) || prepare_ns_cluster(D.d));
 }
 
+// TTT_STAGGER=0 starts every stream group at once (default: staggered).
+bool stagger_on() {
+  static int v = -1;
+  if (v < 0) {
+    const char* s = std::getenv("TTT_STAGGER");
+    v = (s && s[0] == '0') ? 0 : 1;
+  }
+  return v == 1;
+}
+
 // Number of stream groups the (batch, head) sequences are split into: each
 // group's launches cover a contiguous range of sequences on its own stream.
-// TTT_SEQUENCE_GROUPS (1 .. B*H) overrides the default of one group per
-// sequence; 1 runs every launch batched over all sequences on the caller's
-// stream.
+// The default is two groups (measured best on the 760M-scale layer, B*H = 8,
+// among 1, 2, 4 and 8); TTT_SEQUENCE_GROUPS (1 .. B*H) overrides it, and 1
+// runs every launch batched over all sequences on the caller's stream.
 int sequence_groups(const LayerDims& D) {
   const int BH = D.B * D.H;
   if (!per_sequence_streams(D)) return 1;
@@ -421,7 +438,7 @@ int sequence_groups(const LayerDims& D) {
     env = (s && s[0]) ? std::atoi(s) : -1;
   }
   if (env >= 1) return env < BH ? env : BH;
-  return BH;
+  return 2;
 }
 
 int enqueue_all(LayerPlan& L, cudaStream_t st) {
@@ -448,11 +465,17 @@ int enqueue_all(LayerPlan& L, cudaStream_t st) {
   MapCache cache;
   std::vector<cudaStream_t> kids;
   const int groups = sequence_groups(D);
-  if (groups > 1 && stream_pool(groups, &kids)) {
+  std::vector<cudaEvent_t> stagger;
+  if (groups > 1 && stream_pool(groups, &kids) && stagger_events(groups, &stagger)) {
     TTT_CK(fork_streams(st, kids));
+    // Group g starts once group g-1 has its first projections and gradients
+    // enqueued behind it: the groups then alternate between the projection
+    // GEMMs (throughput-bound) and the Newton-Schulz iteration (latency-bound,
+    // a fraction of the SMs) instead of competing in phase.
     for (int g = 0; g < groups; ++g) {
       const int h0 = (int)((long long)BH * g / groups), h1 = (int)((long long)BH * (g + 1) / groups);
-      const int rc = enqueue_range(L, cache, h0, h1 - h0, kids[g]);
+      if (g > 0 && stagger_on()) TTT_CK(cudaStreamWaitEvent(kids[g], stagger[g - 1], 0));
+      const int rc = enqueue_range(L, cache, h0, h1 - h0, kids[g], stagger[g]);
       if (rc != 0) return rc;
     }
     TTT_CK(join_streams(st, kids));

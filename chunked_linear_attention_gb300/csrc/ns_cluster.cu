@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const unsigned long long lim = L.wait_limit_ns;
   const uint32_t tiles_saddr = smem_u32(tiles);
 
-  int s_prod = 0, s_mma = 0, filled = 0, it_mma = 0, it_epi = 0;
+  int s_prod = 0, s_mma = 0, filled = 0, it_mma = 0, it_epi = 0, e_prod = 0;
   uint32_t ph_prod = 0, ph_mma = 0;
   bool ok = true;
   for (int t = 0; t < L.steps; ++t) {
@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const TileCoord tc{0, z, tile / P.tiles_n, tile % P.tiles_n};
             filled += sp.ngroups * (P.K / kBK);
             if (!produce_tile(L.maps, P, sp, tc, tiles, stage_bytes, nstages, full, empty, s_prod,
-                              ph_prod, L.status, lim)) {
+                              ph_prod, 0, 1, e_prod, L.status, lim)) {
               ok = false;
               break;
             }

@@ -309,7 +309,14 @@ __global__ void __launch_bounds__(kPanelThreads, 1)
       }
     } else if (warp == 1) {
       if (lane == 0 && ok) {
-        const uint32_t a_saddr = smem_u32(apanel), r_saddr = smem_u32(ring);
+        // Base descriptors, advanced per operand slice by adding the byte
+        // offset / 16 to the start-address field (shared addresses < 256 KB,
+        // so the 14-bit field cannot carry).  The issue loop stays short: the
+        // tensor core runs only as fast as this thread feeds it.
+        const uint64_t a_desc0 = smem_desc_sw128(smem_u32(apanel), 16, 1024);
+        const uint64_t bk_desc0 = smem_desc_sw128(smem_u32(ring), 16, 1024);     // K-major B
+        const uint64_t bm_desc0 = smem_desc_sw128(smem_u32(ring), 8192, 1024);   // MN-major B
+        const uint32_t stage16 = stage_bytes >> 4;
         for (int p = p_begin; p < p_end && ok; ++p) {
           const int kind = p % 3;
           ok = p == 0 ? mbar_wait(abar, 0, L.status, lim)
@@ -317,22 +324,22 @@ __global__ void __launch_bounds__(kPanelThreads, 1)
           if (!ok) break;
           tc_fence_after();
           const uint32_t idesc = idesc_bf16_f32(half, 0, kind == 2 ? 1 : 0);
+          const uint64_t b_desc0 = kind == 2 ? bm_desc0 : bk_desc0;
+          const uint32_t bkk = kind == 2 ? 2048 / 16 : 32 / 16;   // one 16-deep K slice
           for (int h = 0; h < 2 && ok; ++h) {
+            const uint32_t dcol = tmem + (uint32_t)(h * half);
             for (int ks = 0; ks < nk; ++ks) {
               if (!mbar_wait(&full[s_mma], ph_mma, L.status, lim)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
-              const uint32_t bs = r_saddr + s_mma * stage_bytes;
-              const uint32_t as = a_saddr + ks * kPanelChunk;
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t ad = smem_desc_sw128(as + kk * 32, 16, 1024);
-                const uint64_t bd = kind == 2 ? smem_desc_sw128(bs + kk * 2048, 8192, 1024)
-                                              : smem_desc_sw128(bs + kk * 32, 16, 1024);
-                umma_bf16(tmem + h * half, ad, bd, idesc, (ks | kk) != 0);
-              }
+              const uint64_t ad = a_desc0 + (uint64_t)(ks * (kPanelChunk / 16));
+              const uint64_t bd = b_desc0 + (uint64_t)(s_mma * stage16);
+              umma_bf16(dcol, ad, bd, idesc, ks != 0);
+              umma_bf16(dcol, ad + 2, bd + bkk, idesc, 1);
+              umma_bf16(dcol, ad + 4, bd + 2 * bkk, idesc, 1);
+              umma_bf16(dcol, ad + 6, bd + 3 * bkk, idesc, 1);
               umma_commit_mc(&empty[s_mma], mask);
               if (++s_mma == nstages) {
                 s_mma = 0;
@@ -506,7 +513,7 @@ int launch_ns_panel(MapCache& cache, const NsArgs& a, int* status, unsigned long
   cfg.numAttrs = 1;
   const double n3 = (double)d * d * d;
   const double flops = 3.0 * a.nh * a.steps * 6.0 * n3;
-  ProfScope ps(PT_MUON, stream, flops, 0.0);
+  ProfScope ps(PT_MUON_PANEL, stream, flops, 0.0);
   if (cudaLaunchKernelEx(&cfg, ns_panel_kernel, L) != cudaSuccess) return -6;
   return 0;
 }

@@ -20,6 +20,7 @@ enum ProfTag : int {
   PT_LIN_OUT,
   PT_SELFTEST,
   PT_MUON,
+  PT_MUON_PANEL,
   PT_COUNT
 };
 

@@ -20,6 +20,7 @@ constexpr int kCtrlBytes = 3072;             // barriers, TMEM slot, problem des
 constexpr int kProbOffset = 256;             // problem descriptors inside the control region
 constexpr int kEpiWarps = 12;           // three warps per TMEM lane quarter (column thirds)
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
+constexpr int kProdLanes = 2;           // TMA-issuing lanes of the producer warp
 
 struct TileCoord {
   int prob, z, tm, tn;
@@ -139,14 +140,20 @@ __device__ __forceinline__ void issue_op(const OpCoords& c, uint8_t* dst, int ks
 // TMA producer (one thread): streams every (group, k-step) of one tile through
 // the ring.  `s`/`ph` are the ring position carried across tiles.  Per-operand
 // coordinates live in scalars (no runtime-indexed local arrays in the loop).
+//
+// Several lanes of the producer warp may share the work: every lane walks
+// every ring entry (`e` counts them across tiles) and issues those with
+// e % nlanes == lane, so consecutive entries are in flight from different
+// threads (one thread alone cannot issue TMA fast enough).  nlanes is 1 or 2.
 static __device__ __noinline__ bool produce_tile(const CUtensorMap* maps, const Problem& P,
                                              const SmemPlan& sp, const TileCoord& tc,
                                              uint8_t* tiles, uint32_t stage_bytes, int nstages,
                                              uint64_t* full, uint64_t* empty, int& s,
-                                             uint32_t& ph, int* status, unsigned long long lim) {
+                                             uint32_t& ph, int lane, int nlanes, int& e,
+                                             int* status, unsigned long long lim) {
   const int nk = P.K / kBK;
   const uint32_t b_step = P.bn * kBK * 2;
-  if (P.epi.kind == EPI_GRAD && P.epi.mom) {
+  if (lane == 0 && P.epi.kind == EPI_GRAD && P.epi.mom) {
     // the epilogue reads this tile's momentum rows: bring them into L2 while
     // the main loop runs (whole rows, contiguous)
     const EpiDesc& e = P.epi;
@@ -170,14 +177,16 @@ static __device__ __noinline__ bool produce_tile(const CUtensorMap* maps, const 
     OpCoords cb1 = cb0, cb2 = cb0;
     if (cnt > 1) cb1 = op_coords(maps, P.b[j0 + 1], P.bn, tc.tn * P.bn, tc.z);
     if (cnt > 2) cb2 = op_coords(maps, P.b[j0 + 2], P.bn, tc.tn * P.bn, tc.z);
-    for (int ks = 0; ks < nk; ++ks) {
-      if (!mbar_wait(&empty[s], ph ^ 1, status, lim)) return false;
-      mbar_arrive_expect_tx(&full[s], bytes);
-      uint8_t* st = tiles + s * stage_bytes;
-      issue_op(ca, st, ks, &full[s]);
-      issue_op(cb0, st + kATileBytes, ks, &full[s]);
-      if (cnt > 1) issue_op(cb1, st + kATileBytes + b_step, ks, &full[s]);
-      if (cnt > 2) issue_op(cb2, st + kATileBytes + 2 * b_step, ks, &full[s]);
+    for (int ks = 0; ks < nk; ++ks, ++e) {
+      if ((e & (nlanes - 1)) == lane) {
+        if (!mbar_wait(&empty[s], ph ^ 1, status, lim)) return false;
+        mbar_arrive_expect_tx(&full[s], bytes);
+        uint8_t* st = tiles + s * stage_bytes;
+        issue_op(ca, st, ks, &full[s]);
+        issue_op(cb0, st + kATileBytes, ks, &full[s]);
+        if (cnt > 1) issue_op(cb1, st + kATileBytes + b_step, ks, &full[s]);
+        if (cnt > 2) issue_op(cb2, st + kATileBytes + 2 * b_step, ks, &full[s]);
+      }
       if (++s == nstages) {
         s = 0;
         ph ^= 1;
@@ -224,17 +233,28 @@ static __device__ __noinline__ bool mma_tile(const Problem& P, const SmemPlan& s
     const uint32_t id2 = idesc_bf16_f32(P.bn, a_mn, bmn2);
     const uint32_t d0 = tmem_acc + j0 * P.bn, d1 = d0 + P.bn, d2 = d0 + 2 * P.bn;
     const uint32_t bo0 = kATileBytes, bo1 = kATileBytes + b_step, bo2 = kATileBytes + 2 * b_step;
+    // Stage-0 descriptors, advanced by adding byte offsets / 16 to the start
+    // address field (shared addresses < 256 KB: the 14-bit field never
+    // carries); a 16-deep K slice is 32 B further (K-major) or 2 KB (MN-major).
+    // Keeping this loop short keeps the tensor core fed.
+    const uint64_t a0 = operand_desc(tiles_saddr, a_mn, 0);
+    const uint64_t b0 = operand_desc(tiles_saddr + bo0, bmn0, 0);
+    const uint64_t b1 = operand_desc(tiles_saddr + bo1, bmn1, 0);
+    const uint64_t b2 = operand_desc(tiles_saddr + bo2, bmn2, 0);
+    const uint32_t ka = a_mn ? 128 : 2, kb0 = bmn0 ? 128 : 2, kb1 = bmn1 ? 128 : 2,
+                   kb2 = bmn2 ? 128 : 2;
+    const uint32_t stage16 = stage_bytes >> 4;
     for (int ks = 0; ks < nk; ++ks) {
       if (!mbar_wait(&full[s], ph, status, lim)) return false;
       tc_fence_after();
-      const uint32_t st = tiles_saddr + s * stage_bytes;
+      const uint64_t so = (uint64_t)(s * stage16);
 #pragma unroll
       for (int kk = 0; kk < kBK / 16; ++kk) {
         const uint32_t acc = (ks | kk) != 0;
-        const uint64_t ad = operand_desc(st, a_mn, kk);
-        umma_bf16(d0, ad, operand_desc(st + bo0, bmn0, kk), id0, acc);
-        if (nmma > 1) umma_bf16(d1, ad, operand_desc(st + bo1, bmn1, kk), id1, acc);
-        if (nmma > 2) umma_bf16(d2, ad, operand_desc(st + bo2, bmn2, kk), id2, acc);
+        const uint64_t ad = a0 + so + kk * ka;
+        umma_bf16(d0, ad, b0 + so + kk * kb0, id0, acc);
+        if (nmma > 1) umma_bf16(d1, ad, b1 + so + kk * kb1, id1, acc);
+        if (nmma > 2) umma_bf16(d2, ad, b2 + so + kk * kb2, id2, acc);
       }
       umma_commit(&empty[s]);
       if (++s == nstages) {
