@@ -397,7 +397,7 @@ def run_ours(args):
     cla.profile_start()
     step()
     prof = cla.profile_stop()
-    tc_kernels = ("umma_gemm_kernel", "ns_cluster_kernel", "ns_panel_kernel")
+    tc_kernels = ("umma_gemm_kernel", "ns_cluster_kernel", "ns_panel_kernel", "ns_half_kernel")
     gemm = [p for p in prof if p["kernel"] in tc_kernels]
     g_fl = sum(p["flops"] for p in gemm)
     g_n = sum(p["launches"] for p in gemm)

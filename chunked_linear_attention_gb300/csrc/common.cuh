@@ -160,6 +160,69 @@ __device__ __forceinline__ void sts128(uint32_t saddr, uint4 v) {
                : "memory");
 }
 
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_cluster(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+// Bulk copy of `bytes` (multiple of 16, both ends 16-byte aligned) from this
+// CTA's shared memory to a cluster shared-memory address, completing on the
+// cluster-address mbarrier `mbar_cl` (in the destination CTA).
+__device__ __forceinline__ void bulk_copy_s2c(uint32_t dst_cl, uint32_t src, uint32_t bytes,
+                                              uint32_t mbar_cl) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst_cl), "r"(src), "r"(bytes), "r"(mbar_cl)
+      : "memory");
+}
+
+// Arrive (release, cluster scope) on an mbarrier given by its cluster address.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t mbar_cl) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(mbar_cl)
+               : "memory");
+}
+
+// Store to a cluster shared-memory address.
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr_cl, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr_cl), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_cluster() {
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
+
+// try_wait with acquire at cluster scope (the phase may be completed by other
+// CTAs' release arrivals).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded cluster-scope wait (as mbar_wait).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int* status,
+                                                  unsigned long long limit_ns) {
+  unsigned long long t0 = 0;
+  for (;;) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const unsigned long long now = global_ns();
+    if (t0 == 0) {
+      t0 = now;
+    } else if (now - t0 > limit_ns) {
+      report_status(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
 // Barrier over `count` threads (a multiple of 32) on hardware barrier `id`.
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -290,6 +353,14 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
+}
+
+// The two halves of the cluster barrier, for work between arrival and wait.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // Cluster-wide barrier with release/acquire ordering of memory operations.

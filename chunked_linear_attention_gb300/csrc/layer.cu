@@ -27,6 +27,7 @@
 #include "layer.h"
 #include "exec.h"
 #include "ns_cluster.h"
+#include "ns_half.h"
 #include "ns_panel.h"
 #include "prof.h"
 
@@ -34,16 +35,22 @@ namespace ttt {
 
 namespace {
 
-// Row-panel Newton-Schulz kernel for d % 128 == 0 (d <= 512) unless
-// TTT_NS_PANEL=0; the tile-cluster kernel otherwise.
-bool use_ns_panel(int d) {
-  static int env = -1;
-  if (env < 0) {
-    const char* s = std::getenv("TTT_NS_PANEL");
-    env = (s && s[0] == '0') ? 0 : 1;
+// Newton-Schulz kernel choice for square d x d matrices: the half-panel
+// kernel (d % 128 == 0, d <= 512) by default, the row-panel kernel
+// (d <= 384) with TTT_NS_KERNEL=panel, the tile-cluster kernel with
+// TTT_NS_KERNEL=cluster or when neither applies.
+int ns_kernel_choice() {
+  static int v = -1;
+  if (v < 0) {
+    const char* s = std::getenv("TTT_NS_KERNEL");
+    v = 0;
+    if (s && std::strcmp(s, "panel") == 0) v = 1;
+    if (s && std::strcmp(s, "cluster") == 0) v = 2;
   }
-  return env == 1 && ns_panel_applicable(d);
+  return v;
 }
+bool use_ns_half(int d) { return ns_kernel_choice() == 0 && ns_half_applicable(d); }
+bool use_ns_panel(int d) { return ns_kernel_choice() == 1 && ns_panel_applicable(d); }
 
 
 constexpr size_t kAlign = 256;
@@ -283,7 +290,9 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
       na.ns[0] = D.ns[0];
       na.ns[1] = D.ns[1];
       na.ns[2] = D.ns[2];
-      int rc = use_ns_panel(d) ? launch_ns_panel(cache, na, L.status, L.wait_ns, st) : 1;
+      int rc = 1;
+      if (use_ns_half(d)) rc = launch_ns_half(cache, na, L.status, L.wait_ns, st);
+      if (rc == 1 && use_ns_panel(d)) rc = launch_ns_panel(cache, na, L.status, L.wait_ns, st);
       if (rc == 1) rc = launch_ns_cluster(cache, na, L.status, L.wait_ns, st);
       if (rc < 0) return rc;
       fused_update = rc == 0;
@@ -411,15 +420,18 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
 bool per_sequence_streams(const LayerDims& D) {
   if (!D.bf16 || D.B * D.H < 2) return false;
   if (D.muon_steps == 0) return true;
-  return D.d == D.m && ((use_ns_panel(D.d) && prepare_ns_panel(D.d)) || prepare_ns_cluster(D.d));
+  return D.d == D.m && ((use_ns_half(D.d) && prepare_ns_half(D.d)) ||
+                        (use_ns_panel(D.d) && prepare_ns_panel(D.d)) || prepare_ns_cluster(D.d));
 }
 
-// TTT_STAGGER=0 starts every stream group at once (default: staggered).
+// TTT_STAGGER=1 starts stream group g only after group g-1's first
+// projections and gradients (default: all groups start together, measured
+// slightly faster with the half-panel Newton-Schulz kernel).
 bool stagger_on() {
   static int v = -1;
   if (v < 0) {
     const char* s = std::getenv("TTT_STAGGER");
-    v = (s && s[0] == '0') ? 0 : 1;
+    v = (s && s[0] == '1') ? 1 : 0;
   }
   return v == 1;
 }
@@ -570,6 +582,7 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
   if (tc) {
     if (prepare_umma_gemm() != cudaSuccess) return -6;
     if (muon && d == m) {
+      if (use_ns_half(d)) prepare_ns_half(d);
       if (use_ns_panel(d)) prepare_ns_panel(d);
       prepare_ns_cluster(d);
     }

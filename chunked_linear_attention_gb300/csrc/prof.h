@@ -21,6 +21,7 @@ enum ProfTag : int {
   PT_SELFTEST,
   PT_MUON,
   PT_MUON_PANEL,
+  PT_MUON_HALF,
   PT_COUNT
 };
 
