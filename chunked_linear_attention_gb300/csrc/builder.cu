@@ -69,7 +69,7 @@ void LaunchBuilder::reset() {
 }
 
 OpDesc LaunchBuilder::op(const TensorRef& t, int mn_major, int outer_base, int z_outer,
-                         int box_rows) {
+                         int box_rows, int mn_krows) {
   OpDesc o;
   std::memset(&o, 0, sizeof(o));
   o.mn_major = mn_major;
@@ -86,7 +86,7 @@ OpDesc LaunchBuilder::op(const TensorRef& t, int mn_major, int outer_base, int z
       ok_ = false;
       return o;
     }
-    const int box = mn_major ? 64 : box_rows;
+    const int box = mn_major ? mn_krows : box_rows;
     int slot = -1;
     for (int i = 0; i < nmaps_; ++i)
       if (keys_ptr_[i] == t.ptr && keys_rows_[i] == t.rows && keys_inner_[i] == t.inner &&
@@ -129,6 +129,18 @@ bool LaunchBuilder::add(Problem p) {
     ok_ = false;
     return false;
   }
+  if (tc_ && p.kd == 2) {   // two K steps per stage: one accumulator, K % 128, MN-major boxes
+    bool good = p.K % 128 == 0 && p.nacc == 1;   // 128 K rows deep
+    for (int j = 0; j < p.nacc; ++j) {
+      if (p.a[j].mn_major && keys_box_[p.a[j].map] != 128) good = false;
+      if (p.b[j].mn_major && keys_box_[p.b[j].map] != 128) good = false;
+    }
+    if (!good) {
+      ok_ = false;
+      return false;
+    }
+  }
+  if (!tc_) p.kd = 1;
   const int bm = this->bm();
   if (!tc_) p.bn = kSimtTile;
   p.tiles_m = (p.M + bm - 1) / bm;

@@ -46,7 +46,10 @@ class LaunchBuilder {
   void reset();
   // Operand view: K-major (mn_major = 0) or MN-major; the tile origin of batch
   // z is row outer_base + z * z_outer of `t`.
-  OpDesc op(const TensorRef& t, int mn_major, int outer_base, int z_outer, int box_rows);
+  // MN-major operands load boxes of 64 M/N columns by mn_krows K rows (64, or
+  // 128 for problems with two K steps per stage).
+  OpDesc op(const TensorRef& t, int mn_major, int outer_base, int z_outer, int box_rows,
+            int mn_krows = 64);
   // Tile N size for a problem with `nacc` accumulators and N columns.
   int choose_bn(int N, int nacc) const;
   // Fills tiles and appends.  Returns false when the launch is full.

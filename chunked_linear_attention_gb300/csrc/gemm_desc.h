@@ -72,6 +72,8 @@ struct Problem {
   int a_shared;       // bit j: accumulator j reuses accumulator j-1's A tile
   int tiles_m, tiles_n;
   int tile_start;     // first linear tile index of this problem
+  int kd;             // 64-deep K steps per pipeline stage: 0 or 1, or 2 (MN-major
+                      // operand boxes then span 128 K rows, K-major tiles two boxes)
   OpDesc a[kMaxAcc];
   OpDesc b[kMaxAcc];
   EpiDesc epi;

@@ -225,13 +225,16 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
         const int M = rows_of[s], Nn = cols_of[s];
         const int bn = LB.choose_bn(Nn, 1);
         Problem p = prob0(M, Nn, b, nh, 1, bn);
+        // two 64-deep K steps per stage: 16 KB MN-major boxes instead of 8 KB
+        const int kdg = (tc && b % 128 == 0) ? 2 : 1;
         if (s < 2) {  // g1 = dH1^T K, g3 = dH3^T K  [m, d]
-          p.a[0] = LB.op(s == 0 ? L.TdH1 : L.TdH3, 1, h0 * b, b, 64);
-          p.b[0] = LB.op(L.Tk, 1, h0 * N + up * b, N, 64);
+          p.a[0] = LB.op(s == 0 ? L.TdH1 : L.TdH3, 1, h0 * b, b, 64, 64 * kdg);
+          p.b[0] = LB.op(L.Tk, 1, h0 * N + up * b, N, 64, 64 * kdg);
         } else {      // g2 = V^T P  [d, m]
-          p.a[0] = LB.op(L.Tv, 1, h0 * N + up * b, N, 64);
-          p.b[0] = LB.op(L.TP, 1, h0 * b, b, 64);
+          p.a[0] = LB.op(L.Tv, 1, h0 * N + up * b, N, 64, 64 * kdg);
+          p.b[0] = LB.op(L.TP, 1, h0 * b, b, 64, 64 * kdg);
         }
+        p.kd = kdg;
         p.epi.kind = EPI_GRAD;
         p.epi.out_ld = Nn;
         p.epi.out_z = dm;
@@ -251,6 +254,7 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
       Problem p = prob0(b, d, m, nh, 1, bn);
       p.a[0] = LB.op(L.TAq, 0, h0 * b, b, BM);
       p.b[0] = LB.op(L.TW[2], 0, h0 * d, d, bn);  // W2 [d, m]: N = d rows, K = m contiguous
+      p.kd = (tc && m % 128 == 0) ? 2 : 1;   // same stage size as the gradients
       p.epi.kind = EPI_OUT;
       p.epi.out[0] = static_cast<char*>(a.out) + (long long)h0 * N * d * (long long)ios;
       p.epi.out_ld = d;

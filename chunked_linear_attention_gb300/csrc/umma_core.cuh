@@ -49,6 +49,7 @@ __device__ __forceinline__ TileCoord decode_tile(const Problem* probs, int nprob
 // whose B tiles are of the same major-ness and total N <= 256 is issued as a
 // single MMA (TMEM columns of its accumulators are adjacent).
 struct SmemPlan {
+  int kd;               // 64-deep K steps per stage (1 or 2)
   int ngroups;
   int g_first[kMaxAcc], g_count[kMaxAcc], g_merged[kMaxAcc];
   uint32_t g_bytes[kMaxAcc];
@@ -56,6 +57,7 @@ struct SmemPlan {
 };
 
 __device__ __forceinline__ void plan_problem(const Problem& P, SmemPlan& sp) {
+  sp.kd = P.kd == 2 ? 2 : 1;
   sp.ngroups = 0;
   sp.max_bytes = 0;
   int j = 0;
@@ -69,7 +71,7 @@ __device__ __forceinline__ void plan_problem(const Problem& P, SmemPlan& sp) {
     sp.g_first[g] = j;
     sp.g_count[g] = cnt;
     sp.g_merged[g] = cnt > 1 && same && cnt * P.bn <= 256;
-    sp.g_bytes[g] = kATileBytes + cnt * P.bn * kBK * 2;
+    sp.g_bytes[g] = sp.kd * (kATileBytes + cnt * P.bn * kBK * 2);
     sp.max_bytes = max(sp.max_bytes, sp.g_bytes[g]);
     j += cnt;
   }
@@ -90,6 +92,12 @@ __device__ __forceinline__ void load_operand(const CUtensorMap* maps, const OpDe
   }
 }
 
+// Descriptor of an operand tile at `base` for kd K steps per stage: MN-major
+// blocks of 64 M/N columns are 8 KB x kd apart.
+__device__ __forceinline__ uint64_t operand_desc_kd(uint32_t base, int mn_major, int kd) {
+  return mn_major ? smem_desc_sw128(base, 8192 * kd, 1024) : smem_desc_sw128(base, 16, 1024);
+}
+
 __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int mn_major, int kk) {
   // K-major: a 16-element K slice starts 32 bytes further along the row.
   // MN-major: it starts 16 K-rows (2 KB) further down.
@@ -102,27 +110,34 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int mn_major, in
 // Precomputed TMA coordinates of one operand tile: the k-step ks box(es) are
 // at (x0 + ks * dx, y0 + ks * dy) and, for MN-major operands, nbox boxes of 64
 // M/N columns 64 apart along x.
+//
+// With kd = 2 a stage covers 128 of K: a K-major tile is two boxes of 64 K
+// columns, one after the other (`kbytes` apart), and an MN-major tile's boxes
+// are 128 K rows deep (`bbytes` = 16 KB apart instead of 8 KB).
 struct OpCoords {
   const CUtensorMap* map;
-  int x0, y0, dx, dy, nbox;
+  int x0, y0, dx, dy, nbox, kd, kbytes, bbytes;
 };
 
 __device__ __forceinline__ OpCoords op_coords(const CUtensorMap* maps, const OpDesc& op, int rows,
-                                              int mn0, int z) {
+                                              int mn0, int z, int kd) {
   const int zz = op.z_div > 1 ? z / op.z_div : z;
   OpCoords c;
   c.map = &maps[op.map];
+  c.kd = kd;
+  c.kbytes = rows * kBK * 2;
+  c.bbytes = 8192 * kd;
   if (!op.mn_major) {
     c.x0 = op.inner_base;
     c.y0 = op.outer_base + zz * op.z_outer + mn0;
-    c.dx = kBK;
+    c.dx = kBK * kd;
     c.dy = 0;
     c.nbox = 1;
   } else {
     c.x0 = op.inner_base + mn0;
     c.y0 = op.outer_base + zz * op.z_outer;
     c.dx = 0;
-    c.dy = kBK;
+    c.dy = kBK * kd;
     c.nbox = rows / 64;
   }
   return c;
@@ -130,10 +145,11 @@ __device__ __forceinline__ OpCoords op_coords(const CUtensorMap* maps, const OpD
 
 __device__ __forceinline__ void issue_op(const OpCoords& c, uint8_t* dst, int ks, uint64_t* bar) {
   const int x = c.x0 + ks * c.dx, y = c.y0 + ks * c.dy;
-  if (c.nbox == 1) {
+  if (c.dy == 0) {   // K-major: kd boxes of 64 K columns
     tma_load_2d(dst, c.map, x, y, bar);
+    if (c.kd == 2) tma_load_2d(dst + c.kbytes, c.map, x + kBK, y, bar);
   } else {
-    for (int i = 0; i < c.nbox; ++i) tma_load_2d(dst + i * 8192, c.map, x + i * 64, y, bar);
+    for (int i = 0; i < c.nbox; ++i) tma_load_2d(dst + i * c.bbytes, c.map, x + i * 64, y, bar);
   }
 }
 
@@ -151,8 +167,10 @@ static __device__ __noinline__ bool produce_tile(const CUtensorMap* maps, const 
                                              uint64_t* full, uint64_t* empty, int& s,
                                              uint32_t& ph, int lane, int nlanes, int& e,
                                              int* status, unsigned long long lim) {
-  const int nk = P.K / kBK;
-  const uint32_t b_step = P.bn * kBK * 2;
+  const int kd = sp.kd;
+  const int nk = P.K / (kBK * kd);
+  const uint32_t a_bytes = kATileBytes * kd;
+  const uint32_t b_step = P.bn * kBK * 2 * kd;
   if (lane == 0 && P.epi.kind == EPI_GRAD && P.epi.mom) {
     // the epilogue reads this tile's momentum rows: bring them into L2 while
     // the main loop runs (whole rows, contiguous)
@@ -172,20 +190,20 @@ static __device__ __noinline__ bool produce_tile(const CUtensorMap* maps, const 
   for (int g = 0; g < sp.ngroups; ++g) {
     const int j0 = sp.g_first[g], cnt = sp.g_count[g];
     const uint32_t bytes = sp.g_bytes[g];
-    const OpCoords ca = op_coords(maps, P.a[j0], kBM, tc.tm * kBM, tc.z);
-    const OpCoords cb0 = op_coords(maps, P.b[j0], P.bn, tc.tn * P.bn, tc.z);
+    const OpCoords ca = op_coords(maps, P.a[j0], kBM, tc.tm * kBM, tc.z, kd);
+    const OpCoords cb0 = op_coords(maps, P.b[j0], P.bn, tc.tn * P.bn, tc.z, kd);
     OpCoords cb1 = cb0, cb2 = cb0;
-    if (cnt > 1) cb1 = op_coords(maps, P.b[j0 + 1], P.bn, tc.tn * P.bn, tc.z);
-    if (cnt > 2) cb2 = op_coords(maps, P.b[j0 + 2], P.bn, tc.tn * P.bn, tc.z);
+    if (cnt > 1) cb1 = op_coords(maps, P.b[j0 + 1], P.bn, tc.tn * P.bn, tc.z, kd);
+    if (cnt > 2) cb2 = op_coords(maps, P.b[j0 + 2], P.bn, tc.tn * P.bn, tc.z, kd);
     for (int ks = 0; ks < nk; ++ks, ++e) {
       if ((e & (nlanes - 1)) == lane) {
         if (!mbar_wait(&empty[s], ph ^ 1, status, lim)) return false;
         mbar_arrive_expect_tx(&full[s], bytes);
         uint8_t* st = tiles + s * stage_bytes;
         issue_op(ca, st, ks, &full[s]);
-        issue_op(cb0, st + kATileBytes, ks, &full[s]);
-        if (cnt > 1) issue_op(cb1, st + kATileBytes + b_step, ks, &full[s]);
-        if (cnt > 2) issue_op(cb2, st + kATileBytes + 2 * b_step, ks, &full[s]);
+        issue_op(cb0, st + a_bytes, ks, &full[s]);
+        if (cnt > 1) issue_op(cb1, st + a_bytes + b_step, ks, &full[s]);
+        if (cnt > 2) issue_op(cb2, st + a_bytes + 2 * b_step, ks, &full[s]);
       }
       if (++s == nstages) {
         s = 0;
@@ -217,8 +235,10 @@ static __device__ __noinline__ bool mma_tile(const Problem& P, const SmemPlan& s
                                          uint64_t* full, uint64_t* empty, uint32_t tmem_acc,
                                          int& s, uint32_t& ph, int* status,
                                          unsigned long long lim) {
-  const int nk = P.K / kBK;
-  const uint32_t b_step = P.bn * kBK * 2;
+  const int kd = sp.kd;
+  const int nk = P.K / (kBK * kd);
+  const uint32_t a_bytes = kATileBytes * kd;
+  const uint32_t b_step = P.bn * kBK * 2 * kd;
   for (int g = 0; g < sp.ngroups; ++g) {
     const int j0 = sp.g_first[g], cnt = sp.g_count[g];
     const bool merged = sp.g_merged[g];
@@ -232,29 +252,35 @@ static __device__ __noinline__ bool mma_tile(const Problem& P, const SmemPlan& s
     const uint32_t id1 = idesc_bf16_f32(P.bn, a_mn, bmn1);
     const uint32_t id2 = idesc_bf16_f32(P.bn, a_mn, bmn2);
     const uint32_t d0 = tmem_acc + j0 * P.bn, d1 = d0 + P.bn, d2 = d0 + 2 * P.bn;
-    const uint32_t bo0 = kATileBytes, bo1 = kATileBytes + b_step, bo2 = kATileBytes + 2 * b_step;
+    const uint32_t bo0 = a_bytes, bo1 = a_bytes + b_step, bo2 = a_bytes + 2 * b_step;
     // Stage-0 descriptors, advanced by adding byte offsets / 16 to the start
     // address field (shared addresses < 256 KB: the 14-bit field never
-    // carries); a 16-deep K slice is 32 B further (K-major) or 2 KB (MN-major).
+    // carries); a 16-deep K slice is 32 B further (K-major) or 2 KB (MN-major),
+    // and with kd = 2 the second 64 of K is one K-major tile (rows x 128 B)
+    // further or 8 KB deeper into the MN-major blocks (16 KB apart).
     // Keeping this loop short keeps the tensor core fed.
-    const uint64_t a0 = operand_desc(tiles_saddr, a_mn, 0);
-    const uint64_t b0 = operand_desc(tiles_saddr + bo0, bmn0, 0);
-    const uint64_t b1 = operand_desc(tiles_saddr + bo1, bmn1, 0);
-    const uint64_t b2 = operand_desc(tiles_saddr + bo2, bmn2, 0);
+    const uint64_t a0 = operand_desc_kd(tiles_saddr, a_mn, kd);
+    const uint64_t b0 = operand_desc_kd(tiles_saddr + bo0, bmn0, kd);
+    const uint64_t b1 = operand_desc_kd(tiles_saddr + bo1, bmn1, kd);
+    const uint64_t b2 = operand_desc_kd(tiles_saddr + bo2, bmn2, kd);
     const uint32_t ka = a_mn ? 128 : 2, kb0 = bmn0 ? 128 : 2, kb1 = bmn1 ? 128 : 2,
                    kb2 = bmn2 ? 128 : 2;
+    const uint32_t ha = a_mn ? 512 : kBM * 8, hb0 = bmn0 ? 512 : P.bn * 8;   // next 64 of K
     const uint32_t stage16 = stage_bytes >> 4;
     for (int ks = 0; ks < nk; ++ks) {
       if (!mbar_wait(&full[s], ph, status, lim)) return false;
       tc_fence_after();
       const uint64_t so = (uint64_t)(s * stage16);
+      for (int kh = 0; kh < kd; ++kh) {
+        const uint64_t ah = a0 + so + kh * ha, bh = b0 + so + kh * hb0;
 #pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk) {
-        const uint32_t acc = (ks | kk) != 0;
-        const uint64_t ad = a0 + so + kk * ka;
-        umma_bf16(d0, ad, b0 + so + kk * kb0, id0, acc);
-        if (nmma > 1) umma_bf16(d1, ad, b1 + so + kk * kb1, id1, acc);
-        if (nmma > 2) umma_bf16(d2, ad, b2 + so + kk * kb2, id2, acc);
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          const uint32_t acc = (ks | kh | kk) != 0;
+          const uint64_t ad = ah + kk * ka;
+          umma_bf16(d0, ad, bh + kk * kb0, id0, acc);
+          if (nmma > 1) umma_bf16(d1, ad, b1 + so + kk * kb1, id1, acc);
+          if (nmma > 2) umma_bf16(d2, ad, b2 + so + kk * kb2, id2, acc);
+        }
       }
       umma_commit(&empty[s]);
       if (++s == nstages) {
