@@ -247,6 +247,9 @@ def run_reference(args):
 
 # kernel -> (ncu summary under profiles/, sources whose hash the summary records)
 KERNEL_PROFILE = {
+    "ns_half_kernel": ("profiles/ns_half_kernel_lm760m.md",
+                       ("chunked_linear_attention_gb300/csrc/ns_half.cu",
+                        "chunked_linear_attention_gb300/csrc/common.cuh")),
     "ns_panel_kernel": ("profiles/ns_panel_kernel_lm760m.md",
                         ("chunked_linear_attention_gb300/csrc/ns_panel.cu",
                          "chunked_linear_attention_gb300/csrc/common.cuh")),

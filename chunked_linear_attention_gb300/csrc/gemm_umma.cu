@@ -4,7 +4,7 @@
 //
 // One CTA per SM (the whole 227 KB of shared memory, all 512 TMEM columns)
 // walks the launch's tiles with a static stride of gridDim.x.  Warp roles:
-// two lanes of warp 0 issue TMA loads into a ring of stages, warp 1 issues
+// kProdLanes lanes of warp 0 issue TMA loads into a ring of stages, warp 1 issues
 // tcgen05.mma from one thread, the kEpiWarps warps after them drain TMEM
 // (tcgen05.ld) and run the epilogue.  When a tile needs at most 256 TMEM columns the accumulator is
 // double-buffered, so the epilogue of one tile overlaps the MMAs of the next;

@@ -26,7 +26,7 @@
 // The K loop of every product takes the CTA's own half of the panel first and
 // waits for the partner's half only before the rest.
 //
-// Warp roles (320 threads): warp 0 lanes 0-1 issue the TMA loads, warp 1
+// Warp roles (320 threads): warp 0 lane 0 issues the TMA loads, warp 1
 // lane 0 the tcgen05 MMAs (M = 128, N = d/2), warps 2..9 drain TMEM (warp w
 // reads lanes 32 (w % 4) .., column quarter (w - 2) / 4 of the half).  Every
 // mbarrier wait is bounded and reports TTT_ERR_TIMEOUT; every thread reaches
@@ -48,7 +48,7 @@ constexpr int kHThreads = 320;
 constexpr int kHCtrl = 3072;                 // barriers, TMEM slot, row sums (own [2][128], peer [128])
 constexpr int kHMaxStages = 8;
 constexpr int kHChunk = 128 * 64 * 2;        // one 64-column chunk of a 128-row bf16 panel
-constexpr int kHProdLanes = 2;               // TMA-issuing lanes of warp 0
+constexpr int kHProdLanes = 1;               // TMA-issuing lanes of warp 0 (2 measured no faster)
 
 enum HalfMap : int {
   HM_X0 = 0, HM_X1, HM_G,        // 64 x 64 boxes: B-operand shares

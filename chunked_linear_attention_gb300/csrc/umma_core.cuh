@@ -20,7 +20,7 @@ constexpr int kCtrlBytes = 3072;             // barriers, TMEM slot, problem des
 constexpr int kProbOffset = 256;             // problem descriptors inside the control region
 constexpr int kEpiWarps = 12;           // three warps per TMEM lane quarter (column thirds)
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
-constexpr int kProdLanes = 2;           // TMA-issuing lanes of the producer warp
+constexpr int kProdLanes = 1;           // TMA-issuing lanes of the producer warp (2 measured no faster)
 
 struct TileCoord {
   int prob, z, tm, tn;
