@@ -4,8 +4,8 @@
 //
 // One CTA per SM (the whole 227 KB of shared memory, all 512 TMEM columns)
 // walks the launch's tiles with a static stride of gridDim.x.  Warp roles:
-// kProdLanes lanes of warp 0 issue TMA loads into a ring of stages, warp 1 issues
-// tcgen05.mma from one thread, the kEpiWarps warps after them drain TMEM
+// lane 0 of warps 0 and 2 issue TMA loads into a ring of stages (alternate
+// entries), warp 1 issues tcgen05.mma from one thread, warps 3.. drain TMEM
 // (tcgen05.ld) and run the epilogue.  When a tile needs at most 256 TMEM columns the accumulator is
 // double-buffered, so the epilogue of one tile overlaps the MMAs of the next;
 // the producer always runs ahead into the next tile.  Every wait is bounded
@@ -18,7 +18,10 @@ namespace ttt {
 
 static_assert(sizeof(GemmLaunch) <= 4096, "kernel parameter block too large");
 
-__global__ void __launch_bounds__(kGemmThreads, 1)
+// warp 0 and warp 2: TMA producers; warp 1: MMA issuer; warps 3..: epilogue
+constexpr int kGemmKernelThreads = 96 + 32 * kEpiWarps;
+
+__global__ void __launch_bounds__(kGemmKernelThreads, 1)
     umma_gemm_kernel(const __grid_constant__ GemmLaunch L) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
@@ -43,15 +46,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int i = threadIdx.x; i < words; i += blockDim.x) dw[i] = sw[i];
   }
   const int nprob = L.nprob, total_tiles = L.total_tiles;
+  // each problem's stage plan, computed once (the roles look it up per tile)
+  SmemPlan* plans = reinterpret_cast<SmemPlan*>(smem + kPlanOffset);
+  static_assert(kProbOffset + kMaxProblems * sizeof(Problem) <= kPlanOffset, "control region");
+  static_assert(kPlanOffset + kMaxProblems * sizeof(SmemPlan) <= kCtrlBytes - 64, "control region");
+  __syncthreads();
+  if (threadIdx.x < nprob) plan_problem(probs[threadIdx.x], plans[threadIdx.x]);
   __syncthreads();
 
   // one stage layout for the whole launch: the largest problem's
   uint32_t stage_bytes = 0;
   int max_cols = 0;
   for (int p = 0; p < nprob; ++p) {
-    SmemPlan sp;
-    plan_problem(probs[p], sp);
-    stage_bytes = max(stage_bytes, sp.max_bytes);
+    stage_bytes = max(stage_bytes, plans[p].max_bytes);
     max_cols = max(max_cols, probs[p].nacc * probs[p].bn);
   }
   int nstages = (kUmmaSmemBytes - 1024 - kCtrlBytes - kStagingBytes) / (int)stage_bytes;
@@ -83,21 +90,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const unsigned long long lim = L.wait_limit_ns;
 
-  if (warp == 0) {
-    if (lane < kProdLanes) {
+  if (warp == 0 || warp == 2) {
+    // Two producer threads in different warps share the ring entries round
+    // robin: each thread keeps only a few TMA boxes in flight.
+    if (lane == 0) {
+      const int plane = warp == 0 ? 0 : 1;
       int s = 0, filled = 0, e = 0;
       uint32_t ph = 0;
       for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
         const TileCoord tc = decode_tile(probs, nprob, t);
         const Problem& P = probs[tc.prob];
-        SmemPlan sp;
-        plan_problem(P, sp);
-        filled += sp.ngroups * (P.K / kBK);
+        const SmemPlan& sp = plans[tc.prob];
+        filled += sp.ngroups * (P.K / (kBK * sp.kd));
         if (!produce_tile(L.maps, P, sp, tc, tiles, stage_bytes, nstages, full, empty, s, ph,
-                          lane, kProdLanes, e, L.status, lim))
+                          plane, kProdLanes, e, L.status, lim))
           break;
       }
-      if (lane == 0) drain_producer(full, nstages, s, ph, filled, L.status, lim);
+      if (plane == 0) drain_producer(full, nstages, s, ph, filled, L.status, lim);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -107,8 +116,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
         const TileCoord tc = decode_tile(probs, nprob, t);
         const Problem& P = probs[tc.prob];
-        SmemPlan sp;
-        plan_problem(P, sp);
+        const SmemPlan& sp = plans[tc.prob];
         const int buf = it % nbuf;
         const uint32_t bph = (it / nbuf) & 1;
         if (!mbar_wait(&acce[buf], bph ^ 1, L.status, lim)) break;
@@ -121,7 +129,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     int it = 0;
-    float* stage = staging + (warp - 2) * kStageFloats;
+    const int ew = warp - 3;
+    float* stage = staging + ew * kStageFloats;
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
       const TileCoord tc = decode_tile(probs, nprob, t);
       const Problem& P = probs[tc.prob];
@@ -129,7 +138,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t bph = (it / nbuf) & 1;
       bool ok = false;
       const float sumsq = tc_epilogue_tile(P, tc.z, tc.tm, tc.tn, tmem + buf * 256, &accf[buf], bph,
-                                           L.status, lim, &ok, stage, warp, lane);
+                                           L.status, lim, &ok, stage, warp, ew, lane);
       if (P.epi.kind == EPI_GRAD && P.epi.normsq_out) {
         float ss = sumsq;
 #pragma unroll
@@ -180,7 +189,7 @@ cudaError_t launch_umma_gemm(const GemmLaunch& L, cudaStream_t stream) {
   const int* sm_count = g_sm_count;
   if (L.total_tiles <= 0) return cudaSuccess;
   const int grid = L.total_tiles < sm_count[dev] ? L.total_tiles : sm_count[dev];
-  umma_gemm_kernel<<<grid, kGemmThreads, kUmmaSmemBytes, stream>>>(L);
+  umma_gemm_kernel<<<grid, kGemmKernelThreads, kUmmaSmemBytes, stream>>>(L);
   return cudaGetLastError();
 }
 

@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           bool got = false;
           if (ok)
             tc_epilogue_tile(P, z, tile / P.tiles_n, tile % P.tiles_n, tmem + buf * 256, &accf[buf],
-                             bph, L.status, lim, &got, stage, warp, lane);
+                             bph, L.status, lim, &got, stage, warp, warp - 2, lane);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acce[buf]);

@@ -282,18 +282,20 @@ __device__ __noinline__ float tc_epilogue_blocks(const Problem& P, int tn, uint3
 }
 
 // Epilogue of one tile on the tensor-core path (bf16 work tensors and I/O).
-// `warp` is 2..9; `stage` is this warp's staging block.  Sets *ok_out to the
-// outcome of the (bounded) accumulator wait.  Returns this thread's share of
-// the EPI_GRAD sum of squares.
+// `warp` is the hardware warp index (its TMEM lane quarter is warp % 4), `ew`
+// the epilogue warp index 0 .. kEpiWarps-1 (consecutive warps: every lane
+// quarter gets kEpiWarps / 4 column slices); `stage` is this warp's staging
+// block.  Sets *ok_out to the outcome of the (bounded) accumulator wait.
+// Returns this thread's share of the EPI_GRAD sum of squares.
 __device__ __forceinline__ float tc_epilogue_tile(const Problem& P, int z, int tm, int tn,
                                                   uint32_t tmem_acc, uint64_t* accf,
                                                   uint32_t accf_parity, int* status,
                                                   unsigned long long lim, bool* ok_out,
-                                                  float* stage, int warp, int lane) {
+                                                  float* stage, int warp, int ew, int lane) {
   const EpiDesc& e = P.epi;
   const int sub = warp & 3;
   constexpr int kSplit = kEpiWarps / 4;                 // column slices per lane quarter
-  const int slice = (warp - 2) / 4;
+  const int slice = ew / 4;
   const int bn = P.bn;
   const int row0 = tm * kBM + sub * 32;                 // first row of this warp
   const int rows_valid = min(32, P.M - row0);           // may be <= 0

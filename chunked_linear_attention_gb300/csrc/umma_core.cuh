@@ -18,9 +18,10 @@ constexpr int kATileBytes = kBM * kBK * 2;   // 16 KB
 constexpr int kMaxStages = 8;
 constexpr int kCtrlBytes = 3072;             // barriers, TMEM slot, problem descriptors
 constexpr int kProbOffset = 256;             // problem descriptors inside the control region
+constexpr int kPlanOffset = 2304;            // per-problem stage plans inside the control region
 constexpr int kEpiWarps = 12;           // three warps per TMEM lane quarter (column thirds)
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
-constexpr int kProdLanes = 1;           // TMA-issuing lanes of the producer warp (2 measured no faster)
+constexpr int kProdLanes = 2;           // TMA-issuing threads (lane 0 of two producer warps)
 
 struct TileCoord {
   int prob, z, tm, tn;
@@ -161,7 +162,7 @@ __device__ __forceinline__ void issue_op(const OpCoords& c, uint8_t* dst, int ks
 // every ring entry (`e` counts them across tiles) and issues those with
 // e % nlanes == lane, so consecutive entries are in flight from different
 // threads (one thread alone cannot issue TMA fast enough).  nlanes is 1 or 2.
-static __device__ __noinline__ bool produce_tile(const CUtensorMap* maps, const Problem& P,
+static __device__ __forceinline__ bool produce_tile(const CUtensorMap* maps, const Problem& P,
                                              const SmemPlan& sp, const TileCoord& tc,
                                              uint8_t* tiles, uint32_t stage_bytes, int nstages,
                                              uint64_t* full, uint64_t* empty, int& s,
@@ -230,7 +231,7 @@ __device__ __forceinline__ void drain_producer(uint64_t* full, int nstages, int 
 // MMA issuer (one thread): accumulates one tile into TMEM at column tmem_acc
 // (accumulator j at tmem_acc + j * bn).  Descriptors are scalars built once
 // per group; no runtime-indexed arrays in the k-step loop.
-static __device__ __noinline__ bool mma_tile(const Problem& P, const SmemPlan& sp,
+static __device__ __forceinline__ bool mma_tile(const Problem& P, const SmemPlan& sp,
                                          uint32_t tiles_saddr, uint32_t stage_bytes, int nstages,
                                          uint64_t* full, uint64_t* empty, uint32_t tmem_acc,
                                          int& s, uint32_t& ph, int* status,
