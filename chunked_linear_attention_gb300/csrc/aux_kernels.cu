@@ -42,14 +42,9 @@ struct NormArgs {
   int BH;
   int l2norm;
   long long rows_before[4];  // prefix of BH*rows over the sets
-  float* clear;
-  int clear_n;
 };
 
 __global__ void __launch_bounds__(256) update_normalize_kernel(const __grid_constant__ NormArgs a) {
-  if (blockIdx.x == 0 && a.clear) {
-    for (int i = threadIdx.x; i < a.clear_n; i += blockDim.x) a.clear[i] = 0.f;
-  }
   const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (gw >= a.rows_before[a.nsets]) return;
@@ -89,13 +84,11 @@ __global__ void __launch_bounds__(256) update_normalize_kernel(const __grid_cons
 }
 
 cudaError_t launch_update_normalize(const MatSet* sets, int nsets, int BH, int l2norm,
-                                    float* clear, int clear_n, cudaStream_t stream) {
+                                    cudaStream_t stream) {
   NormArgs a{};
   a.nsets = nsets;
   a.BH = BH;
   a.l2norm = l2norm;
-  a.clear = clear;
-  a.clear_n = clear_n;
   a.rows_before[0] = 0;
   for (int i = 0; i < nsets; ++i) {
     a.sets[i] = sets[i];
@@ -104,6 +97,26 @@ cudaError_t launch_update_normalize(const MatSet* sets, int nsets, int BH, int l
   const long long warps = a.rows_before[nsets];
   const long long blocks = (warps * 32 + 255) / 256;
   update_normalize_kernel<<<(int)(blocks > 0 ? blocks : 1), 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ gradient norms
+// out[s * BH + h] = fixed-order sum of the nslot partials of matrix (s, h),
+// for s = 0..2 and h in [h0, h0 + nh): one warp per matrix.
+__global__ void normsq_reduce_kernel(const float* __restrict__ part, int nslot,
+                                     float* __restrict__ out, int BH, int h0, int nh) {
+  const int w = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  if (w >= 3 * nh) return;
+  const int z = (w / nh) * BH + h0 + w % nh;
+  const float s = sum_partials_warp(part + (long long)z * nslot, nslot);
+  if ((threadIdx.x & 31) == 0) out[z] = s;
+}
+
+cudaError_t launch_normsq_reduce(const float* part, int nslot, float* out, int BH, int h0,
+                                 int nh, cudaStream_t stream) {
+  if (nh <= 0) return cudaSuccess;
+  const int blocks = (3 * nh * 32 + 255) / 256;
+  normsq_reduce_kernel<<<blocks, 256, 0, stream>>>(part, nslot, out, BH, h0, nh);
   return cudaGetLastError();
 }
 

@@ -26,7 +26,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 bool MapCache::get(const TensorRef& t, int box_rows, CUtensorMap* out) {
   for (const Entry& e : entries_)
     if (e.ptr == t.ptr && e.bf16 == t.bf16 && e.rows == t.rows && e.inner == t.inner &&
-        e.box_rows == box_rows) {
+        e.box_rows == box_rows && e.nblk == 0) {
       *out = e.map;
       return true;
     }
@@ -40,6 +40,7 @@ bool MapCache::get(const TensorRef& t, int box_rows, CUtensorMap* out) {
   e.rows = t.rows;
   e.inner = t.inner;
   e.box_rows = box_rows;
+  e.nblk = 0;
   // one 128-byte swizzle row across: 64 bf16 or 32 fp32 elements
   cuuint64_t dims[2] = {(cuuint64_t)t.inner, (cuuint64_t)t.rows};
   cuuint64_t strides[1] = {(cuuint64_t)t.inner * es};
@@ -48,6 +49,36 @@ bool MapCache::get(const TensorRef& t, int box_rows, CUtensorMap* out) {
   CUresult r = fn(&e.map, t.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                   2, const_cast<void*>(t.ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  entries_.push_back(e);
+  *out = e.map;
+  return true;
+}
+
+bool MapCache::get_blocked(const TensorRef& t, int box_rows, int nblk, CUtensorMap* out) {
+  for (const Entry& e : entries_)
+    if (e.ptr == t.ptr && e.bf16 == t.bf16 && e.rows == t.rows && e.inner == t.inner &&
+        e.box_rows == box_rows && e.nblk == nblk) {
+      *out = e.map;
+      return true;
+    }
+  auto fn = encode_fn();
+  if (!fn || !t.bf16 || nblk < 1 || t.inner % 64 != 0) return false;
+  if ((reinterpret_cast<uintptr_t>(t.ptr) & 15) != 0) return false;
+  Entry e;
+  e.ptr = t.ptr;
+  e.bf16 = t.bf16;
+  e.rows = t.rows;
+  e.inner = t.inner;
+  e.box_rows = box_rows;
+  e.nblk = nblk;
+  cuuint64_t dims[3] = {64, (cuuint64_t)t.rows, (cuuint64_t)(t.inner / 64)};
+  cuuint64_t strides[2] = {(cuuint64_t)t.inner * 2, 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)nblk};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(&e.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(t.ptr), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
   entries_.push_back(e);
@@ -124,11 +155,23 @@ int LaunchBuilder::choose_bn(int N, int nacc) const {
   return best;
 }
 
+// True if every row the epilogue reads or writes starts on a 32-byte
+// boundary: row pitch and batch stride multiples of 16 elements (32 bytes of
+// bf16, 64 of fp32) and 32-byte aligned base pointers.
+static bool epi_rows32(const EpiDesc& e) {
+  if (e.out_ld % 16 != 0 || e.out_z % 16 != 0) return false;
+  const void* ptrs[5] = {e.out[0], e.out[1], e.out[2], e.in0, e.mom};
+  for (const void* q : ptrs)
+    if (q && (reinterpret_cast<uintptr_t>(q) & 31) != 0) return false;
+  return true;
+}
+
 bool LaunchBuilder::add(Problem p) {
   if (L_.nprob >= kMaxProblems) {
     ok_ = false;
     return false;
   }
+  p.epi.rows32 = epi_rows32(p.epi) ? 1 : 0;
   if (tc_ && p.kd == 2) {   // two K steps per stage: one accumulator, K % 128, MN-major boxes
     bool good = p.K % 128 == 0 && p.nacc == 1;   // 128 K rows deep
     for (int j = 0; j < p.nacc; ++j) {

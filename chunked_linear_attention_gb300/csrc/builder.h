@@ -26,6 +26,10 @@ struct TensorRef {
 class MapCache {
  public:
   bool get(const TensorRef& t, int box_rows, CUtensorMap* out);
+  // bf16 view read as 64-column blocks: coordinates {column in block, row,
+  // block}; one box is `nblk` consecutive blocks of box_rows rows, landing in
+  // shared memory block after block (MN-major operand atoms of 64 columns).
+  bool get_blocked(const TensorRef& t, int box_rows, int nblk, CUtensorMap* out);
 
  private:
   struct Entry {
@@ -34,6 +38,7 @@ class MapCache {
     long long rows;
     int inner;
     int box_rows;
+    int nblk;   // 0: plain 2-D map
     CUtensorMap map;
   };
   std::vector<Entry> entries_;

@@ -119,6 +119,17 @@ __device__ __forceinline__ void tma_load_2d_mc(void* smem_dst, const CUtensorMap
       : "memory");
 }
 
+// 3-D tiled load of one box, multicast to the CTAs in `cta_mask`.
+__device__ __forceinline__ void tma_load_3d_mc(void* smem_dst, const CUtensorMap* map, int x, int y,
+                                               int w, uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(w), "r"(smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
 // 2-D tiled store of one box from shared memory (bulk async-group).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y,
                                              const void* smem_src) {
@@ -158,6 +169,19 @@ __device__ __forceinline__ void sts128(uint32_t saddr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
                : "memory");
+}
+
+// 32-byte global accesses (eight words at a 32-byte aligned address).
+__device__ __forceinline__ void stg256(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+__device__ __forceinline__ void ldg256(const void* p, uint32_t (&w)[8]) {
+  asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                 "=r"(w[6]), "=r"(w[7])
+               : "l"(p));
 }
 
 // Address of the same shared-memory location in CTA `rank` of the cluster.
@@ -408,6 +432,18 @@ __host__ __device__ __forceinline__ uint32_t idesc_bf16_f32(int n, int a_mn_majo
 // ---------------------------------------------------------------- numerics
 // Fast logistic: hardware exponential and approximate division (a few ulp;
 // large negative x gives 0).
+// Sum of one matrix's squared-norm partials in a fixed order, so that the
+// result is the same on every run: lane i adds slots i, i + 32, ... in turn,
+// then a butterfly over the warp (every lane ends with the same value, since
+// a + b == b + a exactly).  All 32 lanes of the warp must call it.
+__device__ __forceinline__ float sum_partials_warp(const float* part, int n) {
+  float s = 0.f;
+  for (int i = (int)(threadIdx.x & 31); i < n; i += 32) s += part[i];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  return s;
+}
+
 __device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 __device__ __forceinline__ float sigmoid_precise(float x) { return 1.0f / (1.0f + expf(-x)); }
 

@@ -57,10 +57,14 @@ struct EpiDesc {
   long long eta_z;        // elements between batches of eta
   long long eta_row0;     // eta index of the problem's first row
   const float* normsq;    // per-batch sum of squares (Newton-Schulz scale)
-  float* normsq_out;      // per-batch sum of squares accumulated by EPI_GRAD
+  float* normsq_out;      // EPI_GRAD: per-batch partial sums of squares, one slot per
+                          // (tile, warp): slot (tm * tiles_n + tn) * warps + warp of
+                          // batch zz at normsq_out + zz * nslot (plain stores)
+  int nslot;              // partial slots per batch
   float* mom;             // momentum, fp32, same indexing as out
   int z_div;              // batch index of eta / out is z / z_div (0/1 = z)
   int first;              // Newton-Schulz: first step (apply 1/|M|_F)
+  int rows32;             // every output / input row is 32-byte aligned (set by the builder)
   float a, b, c;          // coefficients (NS a, b, c; momentum beta in a)
   float eps;
 };

@@ -86,7 +86,8 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ 
     for (int off = 16; off > 0; off >>= 1) sumsq += __shfl_xor_sync(0xffffffffu, sumsq, off);
     if ((threadIdx.x & 31) == 0) {
       const int zz = P.epi.z_div > 1 ? z / P.epi.z_div : z;
-      atomicAdd(P.epi.normsq_out + zz, sumsq);
+      const int slot = (tm * P.tiles_n + tn) * 8 + (int)(threadIdx.x >> 5);
+      P.epi.normsq_out[(long long)zz * P.epi.nslot + slot] = sumsq;
     }
   }
 }

@@ -21,6 +21,9 @@ static_assert(sizeof(GemmLaunch) <= 4096, "kernel parameter block too large");
 // warp 0 and warp 2: TMA producers; warp 1: MMA issuer; warps 3..: epilogue
 constexpr int kGemmKernelThreads = 96 + 32 * kEpiWarps;
 
+// V8: every problem's epilogue rows are 32-byte aligned (lane-per-row 32-byte
+// accesses); the other instantiation stages rows through shared memory.
+template <bool V8>
 __global__ void __launch_bounds__(kGemmKernelThreads, 1)
     umma_gemm_kernel(const __grid_constant__ GemmLaunch L) {
   extern __shared__ uint8_t smem_raw[];
@@ -137,7 +140,7 @@ __global__ void __launch_bounds__(kGemmKernelThreads, 1)
       const int buf = it % nbuf;
       const uint32_t bph = (it / nbuf) & 1;
       bool ok = false;
-      const float sumsq = tc_epilogue_tile(P, tc.z, tc.tm, tc.tn, tmem + buf * 256, &accf[buf], bph,
+      const float sumsq = tc_epilogue_tile<V8>(P, tc.z, tc.tm, tc.tn, tmem + buf * 256, &accf[buf], bph,
                                            L.status, lim, &ok, stage, warp, ew, lane);
       if (P.epi.kind == EPI_GRAD && P.epi.normsq_out) {
         float ss = sumsq;
@@ -145,7 +148,8 @@ __global__ void __launch_bounds__(kGemmKernelThreads, 1)
         for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
         if (lane == 0) {
           const int zz = P.epi.z_div > 1 ? tc.z / P.epi.z_div : tc.z;
-          atomicAdd(P.epi.normsq_out + zz, ss);
+          const int slot = (tc.tm * P.tiles_n + tc.tn) * kEpiWarps + ew;
+          P.epi.normsq_out[(long long)zz * P.epi.nslot + slot] = ss;
         }
       }
       tc_fence_before();
@@ -171,7 +175,10 @@ cudaError_t prepare_umma_gemm() {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!g_attr_done[dev]) {
-    e = cudaFuncSetAttribute(umma_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(umma_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kUmmaSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(umma_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kUmmaSmemBytes);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
@@ -189,7 +196,12 @@ cudaError_t launch_umma_gemm(const GemmLaunch& L, cudaStream_t stream) {
   const int* sm_count = g_sm_count;
   if (L.total_tiles <= 0) return cudaSuccess;
   const int grid = L.total_tiles < sm_count[dev] ? L.total_tiles : sm_count[dev];
-  umma_gemm_kernel<<<grid, kGemmKernelThreads, kUmmaSmemBytes, stream>>>(L);
+  bool rows32 = true;
+  for (int p = 0; p < L.nprob; ++p) rows32 = rows32 && L.prob[p].epi.rows32;
+  if (rows32)
+    umma_gemm_kernel<true><<<grid, kGemmKernelThreads, kUmmaSmemBytes, stream>>>(L);
+  else
+    umma_gemm_kernel<false><<<grid, kGemmKernelThreads, kUmmaSmemBytes, stream>>>(L);
   return cudaGetLastError();
 }
 

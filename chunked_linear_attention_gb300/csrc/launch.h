@@ -32,10 +32,14 @@ struct MatSet {
 // master = init (broadcast over the batch), work = bf16(master).
 cudaError_t launch_init_weights(const MatSet& m, int B, int H, cudaStream_t stream);
 
-// master = RowNorm(master - update) (or master - update), work = bf16(master);
-// clears `clear_n` floats at `clear` afterwards (Newton-Schulz norms).
+// master = RowNorm(master - update) (or master - update), work = bf16(master).
 cudaError_t launch_update_normalize(const MatSet* sets, int nsets, int BH, int l2norm,
-                                    float* clear, int clear_n, cudaStream_t stream);
+                                    cudaStream_t stream);
+
+// out[s * BH + h] = sum of the nslot partial sums at part + (s * BH + h) * nslot,
+// in a fixed order, for s = 0..2 and h in [h0, h0 + nh).
+cudaError_t launch_normsq_reduce(const float* part, int nslot, float* out, int BH, int h0,
+                                 int nh, cudaStream_t stream);
 
 // dst[i] = src[i] (float), for i < n; src NULL -> zeros.
 cudaError_t launch_copy_f32(float* dst, const float* src, long long n, cudaStream_t stream);

@@ -67,8 +67,15 @@ struct LayerWs {
   void* X[2];
   void* G;
   void* Bm;
-  float* normsq;
+  float* normsq;       // [3][B*H] squared Frobenius norms of M (per-product paths)
+  float* normsq_part;  // [3][B*H][nslot] their partial sums, one per gradient (tile, warp)
+  int nslot;
 };
+
+// Partial-sum slots per matrix for the gradient's squared norm: a bound on
+// (output tiles) x (warps per tile) of either GEMM path (tiles at least
+// 64 x 64, at most 16 warps).  Slots no tile writes stay zero.
+int norm_slots(const LayerDims& D) { return ((D.d + 63) / 64) * ((D.m + 63) / 64) * 16; }
 
 size_t layer_ws_layout(const LayerDims& D, LayerWs* w, char* base) {
   const size_t BH = (size_t)D.B * D.H;
@@ -98,7 +105,9 @@ size_t layer_ws_layout(const LayerDims& D, LayerWs* w, char* base) {
   } else {
     o.X[0] = o.X[1] = o.G = o.Bm = nullptr;
   }
-  o.normsq = reinterpret_cast<float*>(take(3 * BH * 4));
+  o.nslot = norm_slots(D);
+  o.normsq = reinterpret_cast<float*>(take(3 * BH * (1 + (size_t)o.nslot) * 4));
+  o.normsq_part = o.normsq ? o.normsq + 3 * BH : nullptr;
   return off;
 }
 
@@ -242,7 +251,8 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
         p.epi.a = D.beta;
         if (muon) {
           p.epi.out[1] = offs(w.X[0], (long long)s * BH * dm + h0 * dm);
-          p.epi.normsq_out = w.normsq + (long long)s * BH + h0;
+          p.epi.normsq_out = w.normsq_part + ((long long)s * BH + h0) * w.nslot;
+          p.epi.nslot = w.nslot;
         } else if (!L.mom[s]) {
           p.epi.out[0] = w.U + (long long)s * BH * dm + h0 * dm;
         }
@@ -281,6 +291,8 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
       na.Bm = w.Bm;
       na.U = w.U;
       na.normsq = w.normsq;
+      na.normsq_part = w.normsq_part;
+      na.nslot = w.nslot;
       for (int s = 0; s < 3; ++s) {
         na.W[s] = L.ms[s].master;
         na.Wb[s] = L.ms[s].work;
@@ -297,12 +309,16 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
       int rc = 1;
       if (use_ns_half(d)) rc = launch_ns_half(cache, na, L.status, L.wait_ns, st);
       if (rc == 1 && use_ns_panel(d)) rc = launch_ns_panel(cache, na, L.status, L.wait_ns, st);
-      if (rc == 1) rc = launch_ns_cluster(cache, na, L.status, L.wait_ns, st);
+      if (rc == 1) {
+        TTT_CK(launch_normsq_reduce(w.normsq_part, w.nslot, w.normsq, BH, h0, nh, st));
+        rc = launch_ns_cluster(cache, na, L.status, L.wait_ns, st);
+      }
       if (rc < 0) return rc;
       fused_update = rc == 0;
     }
     if (muon && !fused_update) {
       if (h0 != 0 || nh != BH) return -4;   // per-product path runs over all sequences
+      TTT_CK(launch_normsq_reduce(w.normsq_part, w.nslot, w.normsq, BH, 0, BH, st));
       const int sdim = std::min(d, m);
       // groups of equally shaped slots: {0,1,2} if square, else {0,1} and {2}
       int groups[2][2];  // first slot, count
@@ -410,8 +426,7 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
         part[s].update = L.ms[s].update + h0 * rc;
       }
       ProfScope ps(PT_NORM, st, 0.0, 3.0 * nh * dm * (4 + 4 + 4 + (tc ? 2 : 0)));
-      TTT_CK(launch_update_normalize(part, 3, nh, D.l2norm, muon ? w.normsq : nullptr,
-                                     muon ? 3 * BH : 0, st));
+      TTT_CK(launch_update_normalize(part, 3, nh, D.l2norm, st));
     }
   }
   return 0;
@@ -476,7 +491,7 @@ int enqueue_all(LayerPlan& L, cudaStream_t st) {
   }
   {
     ProfScope ps(PT_INIT, st, 0.0, 3.0 * BH * 4);
-    TTT_CK(launch_copy_f32(w.normsq, nullptr, 3LL * BH, st));
+    TTT_CK(launch_copy_f32(w.normsq, nullptr, 3LL * BH * (1 + w.nslot), st));
   }
   MapCache cache;
   std::vector<cudaStream_t> kids;

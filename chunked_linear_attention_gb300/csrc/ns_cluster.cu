@@ -35,7 +35,6 @@ struct NsLaunch {
   Problem gram, poly, step;   // templates for even steps (X0 -> X1)
   const void* X[2];
   float* U;
-  float* normsq;
   float* W[3];                // fp32 state per slot (W1, W3, W2), [B*H][d*d]
   void* Wb[3];                // bf16 operand copies per slot
   int BH, d, steps, cs, l2norm;
@@ -183,7 +182,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t bph = (it_epi >> 1) & 1;
           bool got = false;
           if (ok)
-            tc_epilogue_tile(P, z, tile / P.tiles_n, tile % P.tiles_n, tmem + buf * 256, &accf[buf],
+            tc_epilogue_tile<false>(P, z, tile / P.tiles_n, tile % P.tiles_n, tmem + buf * 256, &accf[buf],
                              bph, L.status, lim, &got, stage, warp, warp - 2, lane);
           tc_fence_before();
           __syncwarp();
@@ -234,7 +233,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     }
-    if (rank == 0 && threadIdx.x == 0) L.normsq[z] = 0.f;
   }
 
   if (warp == 0 && lane == 0) drain_producer(full, nstages, s_prod, ph_prod, filled, L.status, lim);
@@ -369,7 +367,6 @@ int launch_ns_cluster(MapCache& cache, const NsArgs& a, int* status, unsigned lo
   L.X[0] = a.X[0];
   L.X[1] = a.X[1];
   L.U = a.U;
-  L.normsq = a.normsq;
   for (int s = 0; s < 3; ++s) {
     L.W[s] = a.W[s];
     L.Wb[s] = a.Wb[s];

@@ -12,7 +12,9 @@ struct NsArgs {
   void* G;           // bf16 Gram products [3*B*H][d*d]
   void* Bm;          // bf16 polynomial products [3*B*H][d*d]
   float* U;          // fp32 Muon output [3*B*H][d*d]
-  float* normsq;     // squared Frobenius norms of M [3*B*H]
+  float* normsq;     // squared Frobenius norms of M [3*B*H] (per-product paths)
+  const float* normsq_part;  // their partial sums [3*B*H][nslot] (fused kernels)
+  int nslot;
   float* W[3];       // fp32 state per slot (W1, W3, W2)
   void* Wb[3];       // bf16 operand copies per slot
   int BH, d, steps, l2norm;

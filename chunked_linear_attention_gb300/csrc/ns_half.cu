@@ -51,7 +51,9 @@ constexpr int kHChunk = 128 * 64 * 2;        // one 64-column chunk of a 128-row
 constexpr int kHProdLanes = 1;               // TMA-issuing lanes of warp 0 (2 measured no faster)
 
 enum HalfMap : int {
-  HM_X0 = 0, HM_X1, HM_G,        // 64 x 64 boxes: B-operand shares
+  HM_X0 = 0, HM_X1, HM_G,        // 64 x (d/2) boxes: one K slice of a column half (K-major B)
+  HM_X0_MN, HM_X1_MN,            // MN-major B slices: 64 K rows x d/2 columns as R blocks of
+                                 // 64 columns (3-D map), or 64 x 64 shares (2-D, mn_split)
   HM_X0_P, HM_X1_P, HM_G_P,      // 64 x 128 boxes: panel chunks (A load, stores)
   HM_W0, HM_W1, HM_W2,           // fp32 32 x 128 boxes: fast-weight blocks per slot
   HM_COUNT
@@ -59,10 +61,12 @@ enum HalfMap : int {
 
 struct NsHalfLaunch {
   CUtensorMap maps[HM_COUNT];
-  float* normsq;            // squared Frobenius norms of M, cleared at the end
+  const float* normsq_part;  // partial sums of the squared Frobenius norms of M
+  int nslot;                 // partials per matrix
   float* W[3];              // fp32 state per slot (W1, W3, W2), [B*H][d*d]
   void* Wb[3];              // bf16 operand copies per slot
   int BH, d, steps, l2norm, h0, nh, R, nstages;
+  int mn_split;             // MN-major slices fetched as R shares of 64 columns
   float a, b, c, eps;
   int* status;
   unsigned long long wait_limit_ns;
@@ -251,8 +255,9 @@ __global__ void __launch_bounds__(kHThreads, 1)
   const int mrow = z * d;                     // first row of this matrix in the stacked buffers
   const int prow = mrow + r * 128;            // first row of this CTA's panel
   const unsigned long long lim = L.wait_limit_ns;
-  // read before the first cluster barrier; rank 0 clears it at the end
-  const float s1 = 1.0f / (sqrtf(L.normsq[z]) + L.eps);
+  // every warp sums the partials in the same fixed order (same value everywhere)
+  const float s1 =
+      1.0f / (sqrtf(sum_partials_warp(L.normsq_part + (long long)z * L.nslot, L.nslot)) + L.eps);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < nstages; ++s) {
@@ -309,7 +314,9 @@ __global__ void __launch_bounds__(kHThreads, 1)
         for (int p = p_begin; p < p_end && ok; ++p) {
           const int kind = p % 3, tp = p / 3;
           const CUtensorMap* map =
-              kind == 1 ? &L.maps[HM_G] : &L.maps[(tp & 1) ? HM_X1 : HM_X0];
+              kind == 1 ? &L.maps[HM_G]
+                        : &L.maps[kind == 2 ? ((tp & 1) ? HM_X1_MN : HM_X0_MN)
+                                            : ((tp & 1) ? HM_X1 : HM_X0)];
           for (int i = 0; i < nk; ++i) {
             const int ks = i < R ? h * R + i : (1 - h) * R + i - R;   // own half of K first
             if ((issued % kHProdLanes) == lane) {
@@ -318,11 +325,19 @@ __global__ void __launch_bounds__(kHThreads, 1)
                 break;
               }
               mbar_arrive_expect_tx(&full[s_prod], stage_bytes);
-              uint8_t* dst = ring + s_prod * stage_bytes + r * 8192;
-              if (kind == 2)   // X as MN-major B: K = rows of X, N = its columns of half h
-                tma_load_2d_mc(dst, map, h * half + r * 64, mrow + ks * 64, &full[s_prod], hmask);
-              else             // rows of X or G of half h as K-major B
-                tma_load_2d_mc(dst, map, ks * 64, mrow + h * half + r * 64, &full[s_prod], hmask);
+              uint8_t* dst = ring + s_prod * stage_bytes;
+              // one box per K slice, issued in turn by the CTAs of the half and
+              // multicast to all of them
+              const bool mine = i % R == r;
+              if (kind == 2) {   // X as MN-major B: K = rows of X, N = its columns of half h
+                if (L.mn_split)
+                  tma_load_2d_mc(dst + r * 8192, map, h * half + r * 64, mrow + ks * 64,
+                                 &full[s_prod], hmask);
+                else if (mine)
+                  tma_load_3d_mc(dst, map, 0, mrow + ks * 64, h * R, &full[s_prod], hmask);
+              } else if (mine) {   // rows of X or G of half h as K-major B
+                tma_load_2d_mc(dst, map, ks * 64, mrow + h * half, &full[s_prod], hmask);
+              }
             }
             ++issued;   // every producer lane walks every entry
             if (++s_prod == nstages) {
@@ -438,7 +453,6 @@ __global__ void __launch_bounds__(kHThreads, 1)
         }
         if (!got) ok = false;
       }
-      if (iv == nint - 1 && rank == 0 && threadIdx.x == 64) L.normsq[z] = 0.f;
     }
     if (iv + 1 < nint) {
       cluster_arrive();
@@ -524,11 +538,19 @@ int launch_ns_half(MapCache& cache, const NsArgs& a, int* status, unsigned long 
   const struct {
     TensorRef t;
     int box;
-  } maps[HM_COUNT] = {{TX0, 64},  {TX1, 64},  {TG, 64},   {TX0, 128}, {TX1, 128},
-                      {TG, 128},  {TW0, 128}, {TW1, 128}, {TW2, 128}};
-  for (int i = 0; i < HM_COUNT; ++i)
+  } maps[HM_COUNT] = {{TX0, 64 * R}, {TX1, 64 * R}, {TG, 64 * R}, {TX0, 64},  {TX1, 64},
+                      {TX0, 128},    {TX1, 128},    {TG, 128},    {TW0, 128}, {TW1, 128},
+                      {TW2, 128}};
+  // MN-major slices as one 3-D box of R column blocks where the driver takes
+  // the blocked view, else as R shares of 64 columns
+  L.mn_split = !(cache.get_blocked(TX0, 64, R, &L.maps[HM_X0_MN]) &&
+                 cache.get_blocked(TX1, 64, R, &L.maps[HM_X1_MN]));
+  for (int i = 0; i < HM_COUNT; ++i) {
+    if (!L.mn_split && (i == HM_X0_MN || i == HM_X1_MN)) continue;
     if (!cache.get(maps[i].t, maps[i].box, &L.maps[i])) return -4;
-  L.normsq = a.normsq;
+  }
+  L.normsq_part = a.normsq_part;
+  L.nslot = a.nslot;
   for (int s = 0; s < 3; ++s) {
     L.W[s] = a.W[s];
     L.Wb[s] = a.Wb[s];

@@ -53,7 +53,8 @@ enum PanelMap : int {
 
 struct NsPanelLaunch {
   CUtensorMap maps[PM_COUNT];
-  float* normsq;            // squared Frobenius norms of M, cleared at the end
+  const float* normsq_part;  // partial sums of the squared Frobenius norms of M
+  int nslot;                 // partials per matrix
   float* W[3];              // fp32 state per slot (W1, W3, W2), [B*H][d*d]
   void* Wb[3];              // bf16 operand copies per slot
   int BH, d, steps, l2norm, h0, nh, cs, nstages;
@@ -231,8 +232,9 @@ __global__ void __launch_bounds__(kPanelThreads, 1)
   const int prow = mrow + rank * 128;         // first row of this CTA's panel
   const uint16_t mask = (uint16_t)((1u << cs) - 1u);
   const unsigned long long lim = L.wait_limit_ns;
-  // read before the first cluster barrier; rank 0 clears it at the end
-  const float s1 = 1.0f / (sqrtf(L.normsq[z]) + L.eps);
+  // every warp sums the partials in the same fixed order (same value everywhere)
+  const float s1 =
+      1.0f / (sqrtf(sum_partials_warp(L.normsq_part + (long long)z * L.nslot, L.nslot)) + L.eps);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < nstages; ++s) {
@@ -397,7 +399,6 @@ __global__ void __launch_bounds__(kPanelThreads, 1)
         if (e_warp == 0 && lane == 0) mbar_arrive(aready);
         if (!got) ok = false;
       }
-      if (iv == nint - 1 && rank == 0 && threadIdx.x == 64) L.normsq[z] = 0.f;
     }
     if (iv + 1 < nint) cluster_sync_all();
   }
@@ -479,7 +480,8 @@ int launch_ns_panel(MapCache& cache, const NsArgs& a, int* status, unsigned long
                       {TG, 128},  {TW0, 128}, {TW1, 128}, {TW2, 128}};
   for (int i = 0; i < PM_COUNT; ++i)
     if (!cache.get(maps[i].t, maps[i].box, &L.maps[i])) return -4;
-  L.normsq = a.normsq;
+  L.normsq_part = a.normsq_part;
+  L.nslot = a.nslot;
   for (int s = 0; s < 3; ++s) {
     L.W[s] = a.W[s];
     L.Wb[s] = a.Wb[s];

@@ -7,12 +7,14 @@
 //   * per-row scalars (eta, the Newton-Schulz scale) are read once per tile,
 //     and the first input block is requested, before waiting for the
 //     accumulator;
-//   * rows move between a lane's registers and coalesced global accesses
-//     through a 2 KB per-warp staging block in shared memory, in 16-byte
-//     units with an XOR swizzle that keeps both the row-wise and the
-//     coalesced passes free of bank conflicts: a lane packs its row segment
-//     (BW values) into 16-byte units, then the warp stores whole row
-//     segments of consecutive rows with 16-byte vector stores.
+//   * where rows are 32-byte aligned (the usual case), every lane moves its
+//     own row segment of a block (32 bytes of bf16, 64 of fp32) with 32-byte
+//     global loads and stores straight from registers: one instruction per 32
+//     bytes instead of a pass through shared memory;
+//   * otherwise rows move between a lane's registers and coalesced 16-byte
+//     global accesses through a 2 KB per-warp staging block in shared memory,
+//     with an XOR swizzle that keeps both the row-wise and the coalesced
+//     passes free of bank conflicts.
 #pragma once
 
 #include "common.cuh"
@@ -57,11 +59,25 @@ struct BlockIn {
   uint4 w[kU];
 };
 
-// Coalesced global -> registers (rows >= rows_valid read as zero).
-template <typename T, int BW>
+// Global -> registers (rows >= rows_valid read as zero).  V8 (32-byte
+// aligned rows): this lane's own row segment, in order; else coalesced
+// 16-byte units for block_to_row.
+template <typename T, int BW, bool V8>
 __device__ __forceinline__ void block_fetch(const T* base, long long ld, int rows_valid,
                                             BlockIn<T, BW>& g, int lane) {
   constexpr int U = BlockIn<T, BW>::kU;
+  static_assert(U % 2 == 0, "whole 32-byte row segments");
+  if constexpr (V8) {
+    const char* rowp = reinterpret_cast<const char*>(base + (long long)lane * ld);
+#pragma unroll
+    for (int h = 0; h < U / 2; ++h) {
+      uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (lane < rows_valid) ldg256(rowp + 32 * h, w);
+      g.w[2 * h] = make_uint4(w[0], w[1], w[2], w[3]);
+      g.w[2 * h + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+    return;
+  }
 #pragma unroll
   for (int i = 0; i < U; ++i) {
     const int idx = i * 32 + lane, r = idx / U, u = idx % U;
@@ -71,20 +87,25 @@ __device__ __forceinline__ void block_fetch(const T* base, long long ld, int row
   }
 }
 
-// Registers -> staging -> this lane's row (as fp32).
-template <typename T, int BW>
+// Fetched block -> this lane's row (as fp32); through the staging block
+// unless it was fetched lane-per-row (V8).
+template <typename T, int BW, bool V8>
 __device__ __forceinline__ void block_to_row(const BlockIn<T, BW>& g, uint32_t st, float (&x)[BW],
                                              int lane) {
   constexpr int RB = BlockIn<T, BW>::kRB, U = BlockIn<T, BW>::kU;
+  if constexpr (!V8) {
 #pragma unroll
-  for (int i = 0; i < U; ++i) {
-    const int idx = i * 32 + lane;
-    sts128(st + stage_off<RB>(idx / U, idx % U), g.w[i]);
+    for (int i = 0; i < U; ++i) {
+      const int idx = i * 32 + lane;
+      sts128(st + stage_off<RB>(idx / U, idx % U), g.w[i]);
+    }
+    __syncwarp();
   }
-  __syncwarp();
 #pragma unroll
   for (int u = 0; u < U; ++u) {
-    const uint4 w = lds128(st + stage_off<RB>(lane, u));
+    uint4 w;
+    if constexpr (V8) w = g.w[u];
+    else w = lds128(st + stage_off<RB>(lane, u));
     if constexpr (sizeof(T) == 2) {
       x[8 * u + 0] = bf16lo(w.x); x[8 * u + 1] = bf16hi(w.x);
       x[8 * u + 2] = bf16lo(w.y); x[8 * u + 3] = bf16hi(w.y);
@@ -95,14 +116,34 @@ __device__ __forceinline__ void block_to_row(const BlockIn<T, BW>& g, uint32_t s
       x[4 * u + 2] = __uint_as_float(w.z); x[4 * u + 3] = __uint_as_float(w.w);
     }
   }
-  __syncwarp();
+  if constexpr (!V8) __syncwarp();
 }
 
-// This lane's row (BW values) -> staging -> coalesced global stores as T.
-template <typename T, int BW>
+// This lane's row (BW values) -> global as T: with 32-byte stores of the
+// lane's own row where rows are 32-byte aligned (V8), else through the
+// staging block as coalesced 16-byte stores.
+template <typename T, int BW, bool V8>
 __device__ __forceinline__ void store_rows(const float (&v)[BW], uint32_t st, T* base, long long ld,
                                            int rows_valid, int lane) {
   constexpr int RB = BlockIn<T, BW>::kRB, U = BlockIn<T, BW>::kU;
+  if constexpr (V8) {
+    if (lane < rows_valid) {
+      char* rowp = reinterpret_cast<char*>(base + (long long)lane * ld);
+#pragma unroll
+      for (int h = 0; h < RB / 32; ++h) {
+        uint32_t w[8];
+        if constexpr (sizeof(T) == 2) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[16 * h + 2 * i], v[16 * h + 2 * i + 1]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(v[8 * h + i]);
+        }
+        stg256(rowp + 32 * h, w);
+      }
+    }
+    return;
+  }
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     uint4 w;
@@ -137,18 +178,19 @@ constexpr int epi_block_width() {
 // One block of a gradient epilogue: M = beta M + g (momentum present), then
 // the fp32 update source and/or the bf16 Newton-Schulz input with its squared
 // norm.  `x` holds the old momentum when e.mom is set.
+template <bool V8>
 __device__ __forceinline__ float grad_block(const EpiDesc& e, float (&v0)[16], const float (&x)[16],
                                             long long off, int rows_valid, uint32_t st, int lane) {
   float sumsq = 0.f;
   if (e.mom) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v0[i] = e.a * x[i] + v0[i];
-    store_rows<float, 16>(v0, st, e.mom + off, e.out_ld, rows_valid, lane);
+    store_rows<float, 16, V8>(v0, st, e.mom + off, e.out_ld, rows_valid, lane);
   }
   if (e.out[0])
-    store_rows<float, 16>(v0, st, static_cast<float*>(e.out[0]) + off, e.out_ld, rows_valid, lane);
+    store_rows<float, 16, V8>(v0, st, static_cast<float*>(e.out[0]) + off, e.out_ld, rows_valid, lane);
   if (e.out[1]) {
-    store_rows<__nv_bfloat16, 16>(v0, st, static_cast<__nv_bfloat16*>(e.out[1]) + off, e.out_ld,
+    store_rows<__nv_bfloat16, 16, V8>(v0, st, static_cast<__nv_bfloat16*>(e.out[1]) + off, e.out_ld,
                                   rows_valid, lane);
     if (lane < rows_valid) {
 #pragma unroll
@@ -160,8 +202,9 @@ __device__ __forceinline__ float grad_block(const EpiDesc& e, float (&v0)[16], c
 
 // Blocks of one tile for one epilogue kind (the kind is uniform per tile, so
 // each kind is its own non-inlined loop and keeps only the registers it needs).
+// V8: every row the problem touches is 32-byte aligned (decided on the host).
 // Waits (bounded) for the accumulator after requesting the first input block.
-template <int KIND>
+template <int KIND, bool V8>
 __device__ __noinline__ float tc_epilogue_blocks(const Problem& P, int tn, uint32_t tl,
                                                     int c_begin, int c_end, long long tile_base,
                                                     int rows_valid, float eta, float scale,
@@ -184,10 +227,11 @@ __device__ __noinline__ float tc_epilogue_blocks(const Problem& P, int tn, uint3
     const int gcol = tn * bn + c0;
     if (rows_valid <= 0 || gcol >= P.N || x_tmem) return;
     if constexpr (kInBf16)
-      block_fetch(static_cast<const __nv_bfloat16*>(e.in0) + tile_base + gcol, e.out_ld,
-                  rows_valid, gin16, lane);
+      block_fetch<__nv_bfloat16, BW, V8>(static_cast<const __nv_bfloat16*>(e.in0) + tile_base + gcol,
+                                         e.out_ld, rows_valid, gin16, lane);
     if constexpr (kInF32)
-      if (has_mom) block_fetch(e.mom + tile_base + gcol, e.out_ld, rows_valid, gin32, lane);
+      if (has_mom)
+        block_fetch<float, BW, V8>(e.mom + tile_base + gcol, e.out_ld, rows_valid, gin32, lane);
   };
   // the first input block is requested before the accumulator is ready, then
   // inputs run one block ahead
@@ -216,8 +260,8 @@ __device__ __noinline__ float tc_epilogue_blocks(const Problem& P, int tn, uint3
           for (int i = 0; i < BW; ++i) x[i] *= scale * scale;
         }
       } else if (active && (kInBf16 || has_mom)) {
-        if constexpr (kInBf16) block_to_row(gin16, st, x, lane);
-        else block_to_row(gin32, st, x, lane);
+        if constexpr (kInBf16) block_to_row<__nv_bfloat16, BW, V8>(gin16, st, x, lane);
+        else block_to_row<float, BW, V8>(gin32, st, x, lane);
       }
     }
     if (c0 + BW < c_end) prefetch(c0 + BW);
@@ -227,12 +271,12 @@ __device__ __noinline__ float tc_epilogue_blocks(const Problem& P, int tn, uint3
     if (!active) continue;
     const long long off = tile_base + gcol;
     if constexpr (KIND == EPI_STORE_F32) {
-      store_rows<float, BW>(v0, st, static_cast<float*>(e.out[0]) + off, e.out_ld, rows_valid,
+      store_rows<float, BW, V8>(v0, st, static_cast<float*>(e.out[0]) + off, e.out_ld, rows_valid,
                             lane);
     } else if constexpr (KIND == EPI_PROJ_Q) {
 #pragma unroll
       for (int i = 0; i < BW; ++i) v0[i] = v0[i] * sigmoid_f(v0[i]) * v1[i];
-      store_rows<__nv_bfloat16, BW>(v0, st, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
+      store_rows<__nv_bfloat16, BW, V8>(v0, st, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
                                     rows_valid, lane);
     } else if constexpr (KIND == EPI_PROJ_K) {
 #pragma unroll
@@ -245,36 +289,36 @@ __device__ __noinline__ float tc_epilogue_blocks(const Problem& P, int tn, uint3
         v1[i] = dA * sl;                                   // dH3
         v2[i] = -eta * sl * h3;                            // P
       }
-      store_rows<__nv_bfloat16, BW>(v0, st, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
+      store_rows<__nv_bfloat16, BW, V8>(v0, st, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
                                     rows_valid, lane);
-      store_rows<__nv_bfloat16, BW>(v1, st, static_cast<__nv_bfloat16*>(e.out[1]) + off, e.out_ld,
+      store_rows<__nv_bfloat16, BW, V8>(v1, st, static_cast<__nv_bfloat16*>(e.out[1]) + off, e.out_ld,
                                     rows_valid, lane);
-      store_rows<__nv_bfloat16, BW>(v2, st, static_cast<__nv_bfloat16*>(e.out[2]) + off, e.out_ld,
+      store_rows<__nv_bfloat16, BW, V8>(v2, st, static_cast<__nv_bfloat16*>(e.out[2]) + off, e.out_ld,
                                     rows_valid, lane);
     } else if constexpr (KIND == EPI_GRAD) {
-      sumsq += grad_block(e, v0, x, off, rows_valid, st, lane);
+      sumsq += grad_block<V8>(e, v0, x, off, rows_valid, st, lane);
     } else if constexpr (KIND == EPI_OUT) {
-      store_rows<__nv_bfloat16, BW>(v0, st, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
+      store_rows<__nv_bfloat16, BW, V8>(v0, st, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
                                     rows_valid, lane);
     } else if constexpr (KIND == EPI_NS_GRAM) {
       const float s2 = scale * scale;
 #pragma unroll
       for (int i = 0; i < BW; ++i) v0[i] *= s2;
-      store_rows<__nv_bfloat16, BW>(v0, st, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
+      store_rows<__nv_bfloat16, BW, V8>(v0, st, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
                                     rows_valid, lane);
     } else if constexpr (KIND == EPI_NS_POLY) {
 #pragma unroll
       for (int i = 0; i < BW; ++i) v0[i] = e.b * x[i] + e.c * v0[i];
-      store_rows<__nv_bfloat16, BW>(v0, st, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
+      store_rows<__nv_bfloat16, BW, V8>(v0, st, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
                                     rows_valid, lane);
     } else if constexpr (KIND == EPI_NS_STEP) {
 #pragma unroll
       for (int i = 0; i < BW; ++i) v0[i] = scale * (e.a * x[i] + v0[i]);
       if (e.out[1])
-        store_rows<float, BW>(v0, st, static_cast<float*>(e.out[1]) + off, e.out_ld, rows_valid,
+        store_rows<float, BW, V8>(v0, st, static_cast<float*>(e.out[1]) + off, e.out_ld, rows_valid,
                               lane);
       else
-        store_rows<__nv_bfloat16, BW>(v0, st, static_cast<__nv_bfloat16*>(e.out[0]) + off,
+        store_rows<__nv_bfloat16, BW, V8>(v0, st, static_cast<__nv_bfloat16*>(e.out[0]) + off,
                                       e.out_ld, rows_valid, lane);
     }
   }
@@ -286,7 +330,9 @@ __device__ __noinline__ float tc_epilogue_blocks(const Problem& P, int tn, uint3
 // the epilogue warp index 0 .. kEpiWarps-1 (consecutive warps: every lane
 // quarter gets kEpiWarps / 4 column slices); `stage` is this warp's staging
 // block.  Sets *ok_out to the outcome of the (bounded) accumulator wait.
-// Returns this thread's share of the EPI_GRAD sum of squares.
+// Returns this thread's share of the EPI_GRAD sum of squares.  V8: every
+// problem of the launch has 32-byte aligned rows (EpiDesc::rows32).
+template <bool V8>
 __device__ __forceinline__ float tc_epilogue_tile(const Problem& P, int z, int tm, int tn,
                                                   uint32_t tmem_acc, uint64_t* accf,
                                                   uint32_t accf_parity, int* status,
@@ -314,10 +360,10 @@ __device__ __forceinline__ float tc_epilogue_tile(const Problem& P, int z, int t
       e.first)
     scale = ns_scale(e, zz);
 
-#define TTT_EPI_CASE(K)                                                                        \
-  case K:                                                                                      \
-    return tc_epilogue_blocks<K>(P, tn, tl, c_begin, c_end, tile_base, rows_valid, eta, scale, \
-                                 stage, lane, accf, accf_parity, status, lim, ok_out);
+#define TTT_EPI_CASE(K)                                                                       \
+  case K:                                                                                     \
+    return tc_epilogue_blocks<K, V8>(P, tn, tl, c_begin, c_end, tile_base, rows_valid, eta,   \
+                                     scale, stage, lane, accf, accf_parity, status, lim, ok_out);
   switch (e.kind) {
     TTT_EPI_CASE(EPI_STORE_F32)
     TTT_EPI_CASE(EPI_PROJ_Q)

@@ -280,3 +280,38 @@ def test_layer_strided_full_size():
     ref = run_oracle(wl, *inp)
     errs = [rel_l2(g_, r_) for g_, r_ in zip(got, ref[:4])]
     assert max(errs) <= BF16_REL_L2, errs
+
+
+def test_layer_bitwise_repeatable():
+    """Two calls on the same inputs give bit-identical outputs and final weights:
+    the gradient's squared norm (the Newton-Schulz scale) is reduced from
+    per-tile partials in a fixed order, with no floating-point atomics."""
+    cla = lib()
+    wl = dataclasses.replace(W.LM_760M, B=2, H=2, N=2048, chunk=512, muon_steps=5,
+                             momentum_beta=0.9)
+    inp = W.layer_inputs(wl)
+    runs = [run_layer(cla, wl, *inp) for _ in range(2)]
+    for a_, b_ in zip(*runs):
+        assert np.array_equal(a_, b_)
+
+
+def test_layer_output_16_byte_aligned_matches_32():
+    """An output buffer that is 16- but not 32-byte aligned takes the staged
+    epilogue row path (shared-memory transpose, 16-byte stores) instead of the
+    lane-per-row 32-byte stores; the results are bit-identical."""
+    cla = lib()
+    wl = dataclasses.replace(W.LM_760M, B=1, H=2, N=1024, d_h=256, m_h=256, chunk=256,
+                             muon_steps=2, momentum_beta=0.5)
+    q, k, v, eta, W1, W2, W3 = [t.to(DEV) for t in W.layer_inputs(wl)]
+    rule = cla.update_rule(l2norm=wl.l2norm, muon_steps=wl.muon_steps,
+                           momentum_beta=wl.momentum_beta)
+    outs = []
+    for shift in (0, 8):   # bf16 elements: 0 or 16 bytes past a 256-byte aligned base
+        buf = torch.empty(q.numel() + 16, dtype=torch.bfloat16, device=DEV)
+        out = buf[shift:shift + q.numel()].view(q.shape)
+        assert (out.data_ptr() % 32 == 0) == (shift == 0)
+        cla.ttt_layer_forward(q, k, v, eta, W1, W2, W3, wl.chunk, wl.mode, rule, out=out)
+        torch.cuda.synchronize()
+        assert_status_ok(cla)
+        outs.append(out.float().cpu().numpy())
+    assert np.array_equal(outs[0], outs[1])
