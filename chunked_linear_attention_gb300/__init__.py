@@ -32,7 +32,8 @@ EXPORTED = (
     "ttt_status_string", "ttt_layer_workspace_size", "ttt_layer_forward",
     "linattn_workspace_size", "linattn_chunked_forward", "ttt_device_status",
     "ttt_set_wait_limit_ns", "ttt_selftest_gemm", "ttt_launch_count", "ttt_profile_start",
-    "ttt_profile_stop", "linattn_chunked_forward_noalloc",
+    "ttt_profile_stop", "linattn_chunked_forward_noalloc", "ttt_layer_host_workspace_size",
+    "ttt_layer_forward_host",
 )
 
 
@@ -75,6 +76,11 @@ def _declare(lib):
     lib.ttt_layer_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i,
                                       vp, ctypes.POINTER(UpdateRule), vp, vp, vp, vp, vp, vp,
                                       sz, vp]
+    lib.ttt_layer_host_workspace_size.restype = sz
+    lib.ttt_layer_host_workspace_size.argtypes = [i, i, i, i, i, i, i, i,
+                                                  ctypes.POINTER(UpdateRule), i]
+    lib.ttt_layer_forward_host.restype = i
+    lib.ttt_layer_forward_host.argtypes = lib.ttt_layer_forward.argtypes
     lib.linattn_workspace_size.restype = sz
     lib.linattn_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
     lib.linattn_chunked_forward.restype = i
@@ -194,6 +200,68 @@ def ttt_layer_forward(q, k, v, eta, W1, W2, W3, chunk: int, mask_mode: int,
                                0 if workspace is None else workspace.numel(), _stream(stream))
     del keep
     _check(rc, "ttt_layer_forward")
+    return out, W_final[0], W_final[1], W_final[2]
+
+
+def _hptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError("tensors passed to the host-buffer call must be in host memory")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    if not t.is_pinned():
+        raise ValueError("host tensors must be page-locked (tensor.pin_memory())")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def layer_host_workspace_size(B, H, N, d_h, m_h, chunk, io_dtype, mask_mode, rule: UpdateRule,
+                              w_per_batch: int = 0) -> int:
+    return library().ttt_layer_host_workspace_size(B, H, N, d_h, m_h, chunk, io_dtype, mask_mode,
+                                                   ctypes.byref(rule), int(w_per_batch))
+
+
+def ttt_layer_forward_host(q, k, v, eta, W1, W2, W3, chunk: int, mask_mode: int,
+                           rule: Optional[UpdateRule] = None,
+                           update_chunks: Optional[Sequence[int]] = None,
+                           momentum: Optional[torch.Tensor] = None,
+                           out: Optional[torch.Tensor] = None,
+                           W_final: Optional[Sequence[torch.Tensor]] = None,
+                           workspace: Optional[torch.Tensor] = None, stream=None, device=None):
+    """LaCT TTT layer forward on page-locked HOST tensors (see
+    ``ttt_layer_forward_host`` in include/ttt.h): the same shapes as
+    ``ttt_layer_forward``; chunk transfers overlap the kernels.  ``workspace``
+    (a CUDA uint8 tensor) and ``stream`` select the device (else ``device`` or
+    the current one).  Returns (out, W1_final, W2_final, W3_final) host
+    tensors, complete once ``stream`` reaches this point.
+    """
+    lib = library()
+    rule = update_rule() if rule is None else rule
+    B, H, N, d = q.shape
+    m = W1.shape[-2]
+    io = _io_dtype(q)
+    w_per_batch = 1 if W1.dim() == 4 else 0
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    if W_final is None:
+        W_final = (torch.empty((B, H, m, d), dtype=torch.float32, pin_memory=True),
+                   torch.empty((B, H, d, m), dtype=torch.float32, pin_memory=True),
+                   torch.empty((B, H, m, d), dtype=torch.float32, pin_memory=True))
+    dev = workspace.device if workspace is not None else torch.device(
+        "cuda", torch.cuda.current_device() if device is None else torch.device(device).index)
+    ws_bytes = lib.ttt_layer_host_workspace_size(B, H, N, d, m, chunk, io, mask_mode,
+                                                 ctypes.byref(rule), w_per_batch)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
+    keep, fl = _flags(update_chunks, N // chunk if chunk > 0 else 0)
+    with torch.cuda.device(dev):
+        rc = lib.ttt_layer_forward_host(
+            _hptr(q), _hptr(k), _hptr(v), _hptr(eta), _hptr(W1), _hptr(W2), _hptr(W3),
+            w_per_batch, B, H, N, d, m, chunk, io, mask_mode, fl, ctypes.byref(rule), _hptr(out),
+            _hptr(W_final[0]), _hptr(W_final[1]), _hptr(W_final[2]), _hptr(momentum),
+            _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream(stream))
+    del keep
+    _check(rc, "ttt_layer_forward_host")
     return out, W_final[0], W_final[1], W_final[2]
 
 

@@ -82,6 +82,46 @@ int check_lin(int B, int H, int N, int dk, int dv, int chunk, int io, int mode,
   return TTT_OK;
 }
 
+// Device staging of a host-buffer layer call, after the layer workspace
+// (byte offsets into the workspace, 256-byte aligned; room for a separate k
+// and for the momentum whether or not the call uses them).
+struct HostStaging {
+  size_t q, k, v, eta, W[3], out, Wf[3], mom, total;
+};
+
+HostStaging host_staging(const ttt::LayerDims& D, int w_per_batch) {
+  auto al = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t ios = D.bf16 ? 2 : 4, BH = (size_t)D.B * D.H, dm = (size_t)D.d * D.m;
+  const size_t act = BH * D.N * D.d * ios;
+  HostStaging h;
+  size_t off = al(ttt::layer_workspace_bytes(D));
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += al(bytes);
+    return o;
+  };
+  h.q = take(act);
+  h.k = take(act);
+  h.v = take(act);
+  h.eta = take(BH * D.N * 4);
+  for (int i = 0; i < 3; ++i) h.W[i] = take((w_per_batch ? BH : (size_t)D.H) * dm * 4);
+  h.out = take(act);
+  for (int i = 0; i < 3; ++i) h.Wf[i] = take(BH * dm * 4);
+  h.mom = take(3 * BH * dm * 4);
+  h.total = off;
+  return h;
+}
+
+// True if p lies in page-locked host memory (allocated or registered with CUDA).
+bool host_pinned(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeHost;
+}
+
 }  // namespace
 
 extern "C" {
@@ -97,6 +137,7 @@ const char* ttt_status_string(int status) {
     case TTT_ERR_CUDA: return "CUDA runtime error";
     case TTT_ERR_TIMEOUT: return "a kernel's bounded wait ran out";
     case TTT_ERR_ARG: return "argument value out of range";
+    case TTT_ERR_PAGEABLE: return "host buffer not page-locked";
     default: return "unknown status";
   }
 }
@@ -152,6 +193,64 @@ int ttt_layer_forward(const void* q, const void* k, const void* v, const float* 
   a.momentum = momentum;
   a.workspace = workspace;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
+  return ttt::layer_forward(a, D, st, g_wait_limit_ns);
+}
+
+size_t ttt_layer_host_workspace_size(int B, int H, int N, int d_h, int m_h, int chunk,
+                                     int io_dtype, int mask_mode, const ttt_update_rule* rule,
+                                     int w_per_batch) {
+  ttt::LayerDims D;
+  if (check_layer(B, H, N, d_h, m_h, chunk, io_dtype, mask_mode, rule, &D) != TTT_OK) return 0;
+  if (w_per_batch != 0 && w_per_batch != 1) return 0;
+  return host_staging(D, w_per_batch).total;
+}
+
+int ttt_layer_forward_host(const void* q, const void* k, const void* v, const float* eta,
+                           const float* W1, const float* W2, const float* W3, int w_per_batch,
+                           int B, int H, int N, int d_h, int m_h, int chunk, int io_dtype,
+                           int mask_mode, const unsigned char* update_chunks,
+                           const ttt_update_rule* rule, void* out, float* W1_final,
+                           float* W2_final, float* W3_final, float* momentum, void* workspace,
+                           size_t workspace_bytes, ttt_stream_t stream) {
+  if (!q || !k || !v || !eta || !W1 || !W2 || !W3 || !out || !W1_final || !W2_final ||
+      !W3_final || !rule)
+    return TTT_ERR_NULL;
+  ttt::LayerDims D;
+  int rc = check_layer(B, H, N, d_h, m_h, chunk, io_dtype, mask_mode, rule, &D);
+  if (rc != TTT_OK) return rc;
+  if (w_per_batch != 0 && w_per_batch != 1) return TTT_ERR_ARG;
+  if (mask_mode == TTT_STRIDED && !update_chunks) return TTT_ERR_NULL;
+  const void* hptrs[] = {q, k, v, eta, W1, W2, W3, out, W1_final, W2_final, W3_final, momentum};
+  for (const void* p : hptrs)
+    if (p && !host_pinned(p)) return TTT_ERR_PAGEABLE;
+  const HostStaging hs = host_staging(D, w_per_batch);
+  if (!workspace || workspace_bytes < hs.total) return TTT_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return TTT_ERR_ALIGN;
+  int* st = status_ptr();
+  if (!st) return TTT_ERR_CUDA;
+  char* ws = static_cast<char*>(workspace);
+  ttt::HostIO h;
+  h.q = q; h.k = k; h.v = v; h.eta = eta;
+  h.W[0] = W1; h.W[1] = W2; h.W[2] = W3;
+  h.out = out;
+  h.Wf[0] = W1_final; h.Wf[1] = W2_final; h.Wf[2] = W3_final;
+  h.momentum = momentum;
+  ttt::LayerArgs a;
+  a.q = ws + hs.q;
+  a.k = k == q ? a.q : ws + hs.k;
+  a.v = ws + hs.v;
+  a.eta = reinterpret_cast<const float*>(ws + hs.eta);
+  for (int i = 0; i < 3; ++i) {
+    a.W[i] = reinterpret_cast<const float*>(ws + hs.W[i]);
+    a.Wf[i] = reinterpret_cast<float*>(ws + hs.Wf[i]);
+  }
+  a.w_per_batch = w_per_batch;
+  a.update_chunks = update_chunks;
+  a.out = ws + hs.out;
+  a.momentum = momentum ? reinterpret_cast<float*>(ws + hs.mom) : nullptr;
+  a.workspace = workspace;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  a.host = &h;
   return ttt::layer_forward(a, D, st, g_wait_limit_ns);
 }
 

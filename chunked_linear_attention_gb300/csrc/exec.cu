@@ -18,6 +18,7 @@ struct DevicePool {
   std::vector<cudaStream_t> streams;
   std::vector<cudaEvent_t> events;
   std::vector<cudaEvent_t> order_events;
+  std::vector<cudaEvent_t> io_events;
   cudaStream_t capture = nullptr;
 };
 
@@ -85,6 +86,20 @@ bool stagger_events(int n, std::vector<cudaEvent_t>* out) {
     p->order_events.push_back(e);
   }
   out->assign(p->order_events.begin(), p->order_events.begin() + n);
+  return true;
+}
+
+bool io_events(int n, std::vector<cudaEvent_t>* out) {
+  if (n > 4096) return false;
+  std::lock_guard<std::mutex> lk(g_pool_mu);
+  DevicePool* p = pool_for_current();
+  if (!p) return false;
+  while ((int)p->io_events.size() < n) {
+    cudaEvent_t e;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return false;
+    p->io_events.push_back(e);
+  }
+  out->assign(p->io_events.begin(), p->io_events.begin() + n);
   return true;
 }
 

@@ -26,6 +26,10 @@ cudaError_t join_streams(cudaStream_t parent, const std::vector<cudaStream_t>& k
 // (separate from the fork/join events).  Returns false on failure.
 bool stagger_events(int n, std::vector<cudaEvent_t>* out);
 
+// `n` events of the current device for host-transfer ordering (separate from
+// the other pools; n <= 4096).  Returns false on failure.
+bool io_events(int n, std::vector<cudaEvent_t>* out);
+
 // Runs `enqueue(stream)` through a cached graph when possible: on the first
 // call with a given key the launch sequence is captured on an internal stream
 // and instantiated; every call then launches the graph on `stream`.  Falls

@@ -166,10 +166,21 @@ struct LayerPlan {
     if ((x) != cudaSuccess) return -6; \
   } while (0)
 
+// Host-buffer calls: chunk c's inputs are on the device once in_ev[min(c,
+// n_in - 1)] has completed (recorded on the host-to-device stream); a range's
+// output chunks go back on its own device-to-host stream, each ordered after
+// the launch that wrote it.
+struct IoHooks {
+  const cudaEvent_t* in_ev;
+  int n_in;
+  cudaStream_t d2h;
+  cudaEvent_t out_ev;
+};
+
 // `after_first`: if set, recorded on `st` once the first step's projection and
 // gradient launches are enqueued (stream groups start staggered on it).
 int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStream_t st,
-                  cudaEvent_t after_first = nullptr) {
+                  cudaEvent_t after_first = nullptr, const IoHooks* io = nullptr) {
   const LayerArgs& a = *L.a;
   const LayerDims& D = *L.D;
   const LayerWs& w = L.w;
@@ -187,8 +198,13 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
   const int BM = LB.bm();
   const long long bm_h = (long long)b * m;   // activation elements per (batch, head)
 
+  int waited = -1;   // host-buffer calls: last input chunk this stream waited for
   for (const auto& stp : L.steps) {
     const int ap = stp.first, up = stp.second;
+    if (io && std::max(ap, up) > waited) {
+      waited = std::max(ap, up);
+      TTT_CK(cudaStreamWaitEvent(st, io->in_ev[std::min(waited, io->n_in - 1)], 0));
+    }
     // ---------------- PROJ
     if (up >= 0) {
       const int bn = LB.choose_bn(m, 3);
@@ -274,6 +290,15 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
     }
     if (!LB.ok()) return -4;
     TTT_CK(LB.launch(st, PT_GRAD));
+    if (io && ap >= 0) {   // this range's rows of output chunk ap are written: copy them back
+      const size_t row = (size_t)b * d * ios, pitch = (size_t)N * d * ios;
+      const size_t off = ((size_t)h0 * N + (size_t)ap * b) * d * ios;
+      TTT_CK(cudaEventRecord(io->out_ev, st));
+      TTT_CK(cudaStreamWaitEvent(io->d2h, io->out_ev, 0));
+      TTT_CK(cudaMemcpy2DAsync(static_cast<char*>(a.host->out) + off, pitch,
+                               static_cast<const char*>(a.out) + off, pitch, row, nh,
+                               cudaMemcpyDeviceToHost, io->d2h));
+    }
     if (after_first) {
       TTT_CK(cudaEventRecord(after_first, st));
       after_first = nullptr;
@@ -472,14 +497,85 @@ int sequence_groups(const LayerDims& D) {
   return 2;
 }
 
+// Host-buffer calls: chunks [c, c + n) of q, k, v and eta for every
+// sequence, one strided copy per tensor (a row per sequence: n * chunk * width
+// contiguous elements, pitch N * width).
+int copy_in_chunks(const LayerArgs& a, const LayerDims& D, int c, int n, cudaStream_t s) {
+  const HostIO& h = *a.host;
+  const int BH = D.B * D.H;
+  const size_t ios = D.bf16 ? 2 : 4;
+  const size_t row = (size_t)n * D.chunk * D.d * ios, pitch = (size_t)D.N * D.d * ios;
+  const size_t off = (size_t)c * D.chunk * D.d * ios;
+  const void* src[3] = {h.q, h.k, h.v};
+  const void* dst[3] = {a.q, a.k, a.v};
+  for (int i = 0; i < 3; ++i) {
+    if (i == 1 && h.k == h.q) continue;   // k aliases q
+    TTT_CK(cudaMemcpy2DAsync(static_cast<char*>(const_cast<void*>(dst[i])) + off, pitch,
+                             static_cast<const char*>(src[i]) + off, pitch, row, BH,
+                             cudaMemcpyHostToDevice, s));
+  }
+  const size_t erow = (size_t)n * D.chunk * 4, epitch = (size_t)D.N * 4;
+  TTT_CK(cudaMemcpy2DAsync(const_cast<float*>(a.eta) + (size_t)c * D.chunk, epitch,
+                           h.eta + (size_t)c * D.chunk, epitch, erow, BH,
+                           cudaMemcpyHostToDevice, s));
+  return 0;
+}
+
 int enqueue_all(LayerPlan& L, cudaStream_t st) {
   const LayerArgs& a = *L.a;
   const LayerDims& D = *L.D;
   const LayerWs& w = L.w;
+  const HostIO* hio = a.host;
   const bool tc = D.bf16;
   const int BH = D.B * D.H;
+  const int nc = D.N / D.chunk;
   const long long dm = (long long)D.d * D.m;
   const int rows_of[3] = {D.m, D.m, D.d}, cols_of[3] = {D.d, D.d, D.m};
+
+  // streams: [0, ng) compute groups when ng > 1; host-buffer calls add one
+  // host-to-device stream and one device-to-host stream per group
+  int ng = sequence_groups(D);
+  std::vector<cudaStream_t> pool;
+  std::vector<cudaEvent_t> stagger;
+  if (ng > 1 &&
+      !(stream_pool(ng + (hio ? 1 + ng : 0), &pool) && stagger_events(ng, &stagger)))
+    ng = 1;
+  if (ng == 1 && hio && !stream_pool(2, &pool)) return -6;
+  const int io0 = ng > 1 ? ng : 0;
+  std::vector<IoHooks> hooks(ng);
+  std::vector<cudaEvent_t> evs;        // host-buffer calls: input chunks, then one per group
+  std::vector<cudaEvent_t> chunk_ev;   // event of each input chunk
+  if (hio) {
+    std::vector<cudaStream_t> io(pool.begin() + io0, pool.begin() + io0 + 1 + ng);
+    TTT_CK(fork_streams(st, io));   // nothing overwrites staging a prior call still reads
+    const size_t wrows = (size_t)(a.w_per_batch ? D.B : 1) * D.H;
+    for (int s = 0; s < 3; ++s)
+      TTT_CK(cudaMemcpyAsync(const_cast<float*>(a.W[s]), hio->W[s], wrows * dm * 4,
+                             cudaMemcpyHostToDevice, st));
+    if (hio->momentum)
+      TTT_CK(cudaMemcpyAsync(a.momentum, hio->momentum, 3 * (size_t)BH * dm * 4,
+                             cudaMemcpyHostToDevice, st));
+    // every input chunk in order on the host-to-device stream, one event per
+    // chunk (the last event also covers any chunks beyond the pool).  One
+    // strided copy per tensor and chunk runs at the link's full rate; larger
+    // blocks of chunks measured slower overall (the kernels wait longer for
+    // the first chunks of each block).
+    const int nb = std::min(nc, 4096 - ng);
+    if (!io_events(nb + ng, &evs)) return -6;
+    chunk_ev.assign(nc, evs[nb - 1]);
+    for (int c = 0; c < nc; ++c) {
+      const int rc = copy_in_chunks(a, D, c, 1, io[0]);
+      if (rc != 0) return rc;
+      if (c < nb - 1) {
+        TTT_CK(cudaEventRecord(evs[c], io[0]));
+        chunk_ev[c] = evs[c];
+      }
+    }
+    TTT_CK(cudaEventRecord(evs[nb - 1], io[0]));
+    for (int g = 0; g < ng; ++g)
+      hooks[g] = IoHooks{chunk_ev.data(), nc, io[1 + g], evs[nb + g]};
+  }
+
   for (int s = 0; s < 3; ++s) {
     ProfScope ps(PT_INIT, st, 0.0,
                  (double)BH * rows_of[s] * cols_of[s] * (4 + 4 + (tc ? 2 : 0)));
@@ -494,25 +590,35 @@ int enqueue_all(LayerPlan& L, cudaStream_t st) {
     TTT_CK(launch_copy_f32(w.normsq, nullptr, 3LL * BH * (1 + w.nslot), st));
   }
   MapCache cache;
-  std::vector<cudaStream_t> kids;
-  const int groups = sequence_groups(D);
-  std::vector<cudaEvent_t> stagger;
-  if (groups > 1 && stream_pool(groups, &kids) && stagger_events(groups, &stagger)) {
+  if (ng > 1) {
+    std::vector<cudaStream_t> kids(pool.begin(), pool.begin() + ng);
     TTT_CK(fork_streams(st, kids));
-    // Group g starts once group g-1 has its first projections and gradients
-    // enqueued behind it: the groups then alternate between the projection
-    // GEMMs (throughput-bound) and the Newton-Schulz iteration (latency-bound,
-    // a fraction of the SMs) instead of competing in phase.
-    for (int g = 0; g < groups; ++g) {
-      const int h0 = (int)((long long)BH * g / groups), h1 = (int)((long long)BH * (g + 1) / groups);
+    // Group g covers a contiguous range of sequences on its own stream; with
+    // TTT_STAGGER=1 it starts once group g-1 has its first projections and
+    // gradients enqueued.
+    for (int g = 0; g < ng; ++g) {
+      const int h0 = (int)((long long)BH * g / ng), h1 = (int)((long long)BH * (g + 1) / ng);
       if (g > 0 && stagger_on()) TTT_CK(cudaStreamWaitEvent(kids[g], stagger[g - 1], 0));
-      const int rc = enqueue_range(L, cache, h0, h1 - h0, kids[g], stagger[g]);
+      const int rc = enqueue_range(L, cache, h0, h1 - h0, kids[g], stagger[g],
+                                   hio ? &hooks[g] : nullptr);
       if (rc != 0) return rc;
     }
     TTT_CK(join_streams(st, kids));
-    return 0;
+  } else {
+    const int rc = enqueue_range(L, cache, 0, BH, st, nullptr, hio ? &hooks[0] : nullptr);
+    if (rc != 0) return rc;
   }
-  return enqueue_range(L, cache, 0, BH, st);
+  if (hio) {
+    for (int s = 0; s < 3; ++s)
+      TTT_CK(cudaMemcpyAsync(hio->Wf[s], a.Wf[s], (size_t)BH * dm * 4, cudaMemcpyDeviceToHost,
+                             st));
+    if (hio->momentum)
+      TTT_CK(cudaMemcpyAsync(hio->momentum, a.momentum, 3 * (size_t)BH * dm * 4,
+                             cudaMemcpyDeviceToHost, st));
+    std::vector<cudaStream_t> io(pool.begin() + io0, pool.begin() + io0 + 1 + ng);
+    TTT_CK(join_streams(st, io));
+  }
+  return 0;
 }
 
 #undef TTT_CK
@@ -597,6 +703,14 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
       fbits(D.ns[0]), fbits(D.ns[1]),
       fbits(D.ns[2]), (uint64_t)status, (uint64_t)wait_ns};
   key.insert(key.end(), flagbits.begin(), flagbits.end());
+  if (a.host) {   // host-buffer call: the host tensors too
+    const HostIO& h = *a.host;
+    const void* hp[11] = {h.q, h.k, h.v, h.eta, h.W[0], h.W[1], h.W[2],
+                          h.out, h.Wf[0], h.Wf[1], h.Wf[2]};
+    key.push_back(0x686f7374ull);
+    for (const void* p : hp) key.push_back((uint64_t)p);
+    key.push_back((uint64_t)h.momentum);
+  }
   // one-time device setup outside any capture
   if (tc) {
     if (prepare_umma_gemm() != cudaSuccess) return -6;

@@ -18,6 +18,21 @@ struct LayerDims {
   float ns[3];
 };
 
+// Page-locked host tensors of a host-buffer call: the layer copies each
+// chunk's q, k, v, eta into the device tensors of LayerArgs on a copy stream
+// just ahead of the launches that read it, copies each chunk's output back as
+// soon as it is written, and the weights in before and out after the scan.
+struct HostIO {
+  const void* q;
+  const void* k;       // may equal q (then LayerArgs::k equals LayerArgs::q)
+  const void* v;
+  const float* eta;
+  const float* W[3];   // W1, W2, W3
+  void* out;
+  float* Wf[3];        // W1_final, W2_final, W3_final
+  float* momentum;     // or NULL
+};
+
 struct LayerArgs {
   const void* q;
   const void* k;
@@ -31,6 +46,7 @@ struct LayerArgs {
   float* momentum;     // [3][B*H][d*m] (M1, M2, M3) or NULL
   void* workspace;
   cudaStream_t stream;
+  const HostIO* host = nullptr;   // set: the device tensors above are staging copies
 };
 
 size_t layer_workspace_bytes(const LayerDims& D);

@@ -50,7 +50,8 @@ typedef enum {
   TTT_ERR_WORKSPACE = -5,   /* workspace NULL or smaller than the query says */
   TTT_ERR_CUDA = -6,        /* a CUDA runtime call failed (no device, launch) */
   TTT_ERR_TIMEOUT = -7,     /* a kernel's bounded wait ran out (device word) */
-  TTT_ERR_ARG = -8          /* an argument value is out of range */
+  TTT_ERR_ARG = -8,         /* an argument value is out of range */
+  TTT_ERR_PAGEABLE = -9     /* a host buffer is not page-locked */
 } ttt_status;
 
 typedef enum { TTT_F32 = 0, TTT_BF16 = 1 } ttt_dtype;
@@ -132,6 +133,42 @@ int ttt_layer_forward(const void* q, const void* k, const void* v, const float* 
                       void* out, float* W1_final, float* W2_final, float* W3_final,
                       float* momentum, void* workspace, size_t workspace_bytes,
                       ttt_stream_t stream);
+
+/* Bytes of device workspace ttt_layer_forward_host needs (0 if the arguments
+ * are invalid): the layer workspace plus device copies of q, k, v, eta, the
+ * initial and final weights, the momentum and out. */
+size_t ttt_layer_host_workspace_size(int B, int H, int N, int d_h, int m_h, int chunk,
+                                     int io_dtype, int mask_mode,
+                                     const ttt_update_rule* rule, int w_per_batch);
+
+/* ttt_layer_forward with every tensor in page-locked HOST memory (allocated
+ * with cudaHostAlloc / cudaMallocHost or registered with cudaHostRegister):
+ * the same arguments, shapes, results and support as ttt_layer_forward, with
+ * q, k, v, eta, W1, W2, W3, out, W1_final, W2_final, W3_final and momentum
+ * host pointers (k may equal q; momentum may be NULL).
+ *
+ * The call copies the weights (and momentum) to the device, then each chunk
+ * of q, k, v, eta for all (batch, head) sequences on a copy stream, in chunk
+ * order; the layer's launches for a chunk wait only for that chunk's copy,
+ * and each chunk's output rows go back to host memory as soon as they are
+ * written, so transfers in both directions overlap the kernels.  The final
+ * weights (and momentum) are copied back after the last chunk.  Everything
+ * is ordered on `stream`: the host results are complete when work enqueued
+ * after the call on `stream` runs (e.g. after cudaStreamSynchronize).
+ *
+ *   workspace  device scratch of at least ttt_layer_host_workspace_size()
+ *              bytes, 256-byte aligned, not shared with a concurrent call.
+ *
+ * Returns TTT_ERR_PAGEABLE if a host buffer is not page-locked, otherwise the
+ * codes of ttt_layer_forward. */
+int ttt_layer_forward_host(const void* q, const void* k, const void* v, const float* eta,
+                           const float* W1, const float* W2, const float* W3, int w_per_batch,
+                           int B, int H, int N, int d_h, int m_h, int chunk, int io_dtype,
+                           int mask_mode, const unsigned char* update_chunks,
+                           const ttt_update_rule* rule,
+                           void* out, float* W1_final, float* W2_final, float* W3_final,
+                           float* momentum, void* workspace, size_t workspace_bytes,
+                           ttt_stream_t stream);
 
 /* Bytes of device workspace linattn_chunked_forward needs (0 if invalid). */
 size_t linattn_workspace_size(int B, int H, int N, int d_k, int d_v, int chunk,

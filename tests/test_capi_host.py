@@ -13,6 +13,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 TTT_OK, TTT_ERR_NULL, TTT_ERR_SHAPE, TTT_ERR_ALIGN = 0, -1, -2, -3
 TTT_ERR_UNSUPPORTED, TTT_ERR_WORKSPACE, TTT_ERR_CUDA, TTT_ERR_ARG = -4, -5, -6, -8
+TTT_ERR_PAGEABLE = -9
 
 
 @pytest.fixture(scope="module")
@@ -47,7 +48,7 @@ def test_exports_every_declared_symbol(cla):
 
 
 def test_status_strings(cla):
-    for code in (0, -1, -2, -3, -4, -5, -6, -7, -8):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, -8, -9):
         s = cla.status_string(code)
         assert s and s != "unknown status"
     assert cla.status_string(12345) == "unknown status"
@@ -138,3 +139,50 @@ def test_binding_refuses_cpu_tensors(cla):
     with pytest.raises((ValueError, RuntimeError)):
         cla.ttt_layer_forward(q, q, q, eta, W1, W1, W1, 128, cla.APPLY_THEN_UPDATE,
                               W_final=(W1, W1, W1), workspace=torch.zeros(16, dtype=torch.uint8))
+
+
+def call_layer_host(cla, B=1, H=1, N=256, d=64, m=64, chunk=128, io=1, mode=0, flags=None,
+                    nulls=(), ws_bytes=None, w_per_batch=0):
+    lib = cla.library()
+    rule = cla.update_rule()
+    need = lib.ttt_layer_host_workspace_size(B, H, N, d, m, chunk, io, mode, ctypes.byref(rule),
+                                             w_per_batch)
+    ptrs = [fake(0x100000 * (i + 1)) for i in range(12)]
+    for i in nulls:
+        ptrs[i] = None
+    q, k, v, eta, W1, W2, W3, out, F1, F2, F3, ws_ptr = ptrs
+    return lib.ttt_layer_forward_host(q, k, v, eta, W1, W2, W3, w_per_batch, B, H, N, d, m, chunk,
+                                      io, mode, flags, ctypes.byref(rule), out, F1, F2, F3, None,
+                                      ws_ptr, need if ws_bytes is None else ws_bytes, None)
+
+
+def test_layer_host_call_checks_arguments_and_page_locking(cla):
+    assert call_layer_host(cla, nulls=(0,)) == TTT_ERR_NULL
+    assert call_layer_host(cla, N=300) == TTT_ERR_SHAPE
+    assert call_layer_host(cla, d=100) == TTT_ERR_UNSUPPORTED
+    assert call_layer_host(cla, w_per_batch=2) == TTT_ERR_ARG
+    assert call_layer_host(cla, mode=3) == TTT_ERR_NULL
+    # valid sizes, but these host addresses are not page-locked allocations
+    assert call_layer_host(cla) == TTT_ERR_PAGEABLE
+
+
+def test_layer_host_workspace_adds_device_staging(cla):
+    lib = cla.library()
+    r = cla.update_rule(muon_steps=5, momentum_beta=0.9)
+    B, H, N, d, m = 2, 4, 4096, 384, 384
+    dev = lib.ttt_layer_workspace_size(B, H, N, d, m, 2048, 1, 0, ctypes.byref(r))
+    host = lib.ttt_layer_host_workspace_size(B, H, N, d, m, 2048, 1, 0, ctypes.byref(r), 0)
+    act = B * H * N * d * 2
+    # q, k, v and out staging at least
+    assert host >= dev + 4 * act
+    assert lib.ttt_layer_host_workspace_size(B, H, N, d, m, 2048, 1, 0, ctypes.byref(r), 5) == 0
+
+
+def test_host_binding_refuses_device_or_pageable_tensors(cla):
+    q = torch.zeros(1, 1, 256, 64, dtype=torch.bfloat16)
+    eta = torch.zeros(1, 1, 256)
+    W1 = torch.zeros(1, 64, 64)
+    with pytest.raises((ValueError, RuntimeError)):
+        cla.ttt_layer_forward_host(q, q, q, eta, W1, W1, W1, 128, cla.APPLY_THEN_UPDATE,
+                                   out=q, W_final=(W1, W1, W1),
+                                   workspace=torch.zeros(16, dtype=torch.uint8))

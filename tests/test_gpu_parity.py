@@ -315,3 +315,55 @@ def test_layer_output_16_byte_aligned_matches_32():
         assert_status_ok(cla)
         outs.append(out.float().cpu().numpy())
     assert np.array_equal(outs[0], outs[1])
+
+
+HOST_CASES = [
+    # two stream groups, Muon, momentum; k is the same tensor as q
+    dict(wl=dict(B=2, H=2, N=2048, d_h=256, m_h=256, chunk=512, muon_steps=5,
+                 momentum_beta=0.9), k_is_q=True, momentum=False, per_batch=False),
+    # strided update flags, carried momentum, per-batch initial weights
+    dict(wl=dict(B=1, H=2, N=1024, d_h=128, m_h=256, chunk=128, muon_steps=0,
+                 momentum_beta=0.5, mode=W.STRIDED,
+                 update_chunks=(1, 0, 0, 1, 0, 1, 1, 0)), k_is_q=False, momentum=True,
+         per_batch=True),
+]
+
+
+@pytest.mark.parametrize("case", HOST_CASES)
+def test_layer_host_buffers_match_device_call(case):
+    """The host-buffer call (chunk copies overlapped with the kernels) returns
+    exactly what the device call returns on the same inputs."""
+    cla = lib()
+    wl = dataclasses.replace(W.LM_760M, **case["wl"])
+    q, k, v, eta, W1, W2, W3 = W.layer_inputs(wl)
+    if case["k_is_q"]:
+        k = q
+    if case["per_batch"]:
+        W1, W2, W3 = [w.unsqueeze(0).expand(wl.B, *w.shape).contiguous() for w in (W1, W2, W3)]
+    B, H, d, m = wl.B, wl.H, wl.d_h, wl.m_h
+    mom = torch.randn(3, B, H, m * d, generator=torch.Generator().manual_seed(3)) * 0.01
+    rule = cla.update_rule(l2norm=wl.l2norm, muon_steps=wl.muon_steps,
+                           momentum_beta=wl.momentum_beta)
+    # device call
+    dmom = mom.to(DEV) if case["momentum"] else None
+    dk = None if case["k_is_q"] else k.to(DEV)
+    dq = q.to(DEV)
+    ref = cla.ttt_layer_forward(dq, dq if dk is None else dk, v.to(DEV), eta.to(DEV), W1.to(DEV),
+                                W2.to(DEV), W3.to(DEV), wl.chunk, wl.mode, rule,
+                                update_chunks=wl.update_chunks, momentum=dmom)
+    torch.cuda.synchronize()
+    assert_status_ok(cla)
+    ref = [t.cpu() for t in ref]
+    # host call on page-locked copies
+    hq, hv, heta = q.pin_memory(), v.pin_memory(), eta.pin_memory()
+    hk = hq if case["k_is_q"] else k.pin_memory()
+    hW = [w.pin_memory() for w in (W1, W2, W3)]
+    hmom = mom.clone().pin_memory() if case["momentum"] else None
+    got = cla.ttt_layer_forward_host(hq, hk, hv, heta, *hW, wl.chunk, wl.mode, rule,
+                                     update_chunks=wl.update_chunks, momentum=hmom)
+    torch.cuda.synchronize()
+    assert_status_ok(cla)
+    for g_, r_ in zip(got, ref):
+        assert torch.equal(g_, r_)
+    if case["momentum"]:
+        assert torch.equal(hmom, dmom.cpu())
