@@ -444,7 +444,14 @@ __device__ __forceinline__ float sum_partials_warp(const float* part, int n) {
   return s;
 }
 
-__device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+// sigmoid(x) = (1 + tanh(x / 2)) / 2 with the hardware tanh approximation: one
+// special-function operation per element instead of an exponential and a
+// reciprocal (the epilogues that apply SiLU are bound by those).
+__device__ __forceinline__ float sigmoid_f(float x) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
+  return fmaf(0.5f, t, 0.5f);
+}
 __device__ __forceinline__ float sigmoid_precise(float x) { return 1.0f / (1.0f + expf(-x)); }
 
 template <typename T>
