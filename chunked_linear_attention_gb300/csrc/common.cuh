@@ -430,8 +430,6 @@ __host__ __device__ __forceinline__ uint32_t idesc_bf16_f32(int n, int a_mn_majo
 }
 
 // ---------------------------------------------------------------- numerics
-// Fast logistic: hardware exponential and approximate division (a few ulp;
-// large negative x gives 0).
 // Sum of one matrix's squared-norm partials in a fixed order, so that the
 // result is the same on every run: lane i adds slots i, i + 32, ... in turn,
 // then a butterfly over the warp (every lane ends with the same value, since

@@ -15,6 +15,7 @@
 
 #include "builder.h"
 #include "layer.h"
+#include "linattn_fused.h"
 #include "linattn_kernels.h"
 #include "prof.h"
 
@@ -25,14 +26,18 @@ namespace {
 constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
+// Token splits of each chunk's state sum: enough tiles for one wave over the
+// SMs, each split at least 512 tokens and a multiple of 128 (two 64-deep K
+// steps per pipeline stage); fewer splits also mean fewer fp32 partials for
+// the prefix pass to read.
 int choose_splits(const LinDims& D, int tiles_per_z) {
   const long long pairs = (long long)D.B * D.H * (D.N / D.chunk);
   int splits = 1;
-  while (pairs * splits * tiles_per_z < 2 * 152) {
+  while (pairs * splits * tiles_per_z < 152) {
     const int next = splits * 2;
     if (D.chunk % next != 0) break;
     const int len = D.chunk / next;
-    if (len < 256 || len % 64 != 0) break;
+    if (len < 512 || len % 128 != 0) break;
     splits = next;
   }
   return splits;
@@ -82,16 +87,21 @@ Problem prob0(int M, int N, int K, int Z, int nacc, int bn) {
 
 }  // namespace
 
-size_t linattn_workspace_bytes(const LinDims& D) { return lin_layout(D, nullptr, nullptr); }
+// Room for either path: the one-launch kernel where it applies, the
+// multi-launch path otherwise (and as the fallback on devices without
+// cooperative launch).
+size_t linattn_workspace_bytes(const LinDims& D) {
+  size_t n = lin_layout(D, nullptr, nullptr);
+  if (linattn_fused_applicable(D))
+    n = std::max(n, linattn_fused_scratch(D, linattn_fused_plan(D)));
+  return n;
+}
 
 int linattn_forward(const LinArgs& a, const LinDims& D, int* status, unsigned long long wait_ns) {
-  LinWs w;
-  lin_layout(D, &w, static_cast<char*>(a.workspace));
   cudaStream_t st = a.stream;
   const bool tc = D.bf16;
   const int BH = D.B * D.H, N = D.N, dk = D.dk, dv = D.dv, b = D.chunk;
   const int nc = N / b;
-  const int splits = w.splits, slen = b / splits;
   const int wb16 = tc ? 1 : 0;
 
   UpdateFlags flags;
@@ -101,6 +111,26 @@ int linattn_forward(const LinArgs& a, const LinDims& D, int* status, unsigned lo
     for (int c = 0; c < nc; ++c)
       if (a.update_chunks[c]) flags.bits[c >> 5] |= 1u << (c & 31);
 
+  if (linattn_fused_applicable(D)) {
+    MapCache fcache;
+    LinFusedArgs fa;
+    fa.D = &D;
+    fa.q = a.q;
+    fa.k = a.k;
+    fa.v = a.v;
+    fa.eta = a.eta;
+    fa.S0 = a.S0;
+    fa.flags = &flags;
+    fa.out = a.out;
+    fa.S_final = a.S_final;
+    fa.scratch = a.workspace;
+    const int rc = launch_linattn_fused(fcache, fa, status, wait_ns, st);
+    if (rc <= 0) return rc;
+  }
+
+  LinWs w;
+  lin_layout(D, &w, static_cast<char*>(a.workspace));
+  const int splits = w.splits, slen = b / splits;
   {
     const size_t es = tc ? 2 : 4;
     ProfScope ps(PT_LIN_SCALE, st, 0.0, (double)BH * N * (dv * es * 2 + 4));
@@ -119,8 +149,11 @@ int linattn_forward(const LinArgs& a, const LinDims& D, int* status, unsigned lo
   {  // partial states
     const int bn = LB.choose_bn(dk, 1);
     Problem p = prob0(dv, dk, slen, BH * nc * splits, 1, bn);
-    p.a[0] = LB.op(TVt, 1, 0, slen, 64);
-    p.b[0] = LB.op(Tk, 1, 0, slen, 64);
+    // MN-major operands (token rows): 16 KB boxes of 128 K rows when the split allows
+    const int kd = (tc && slen % 128 == 0) ? 2 : 1;
+    p.a[0] = LB.op(TVt, 1, 0, slen, 64, 64 * kd);
+    p.b[0] = LB.op(Tk, 1, 0, slen, 64, 64 * kd);
+    p.kd = kd;
     p.epi.kind = EPI_STORE_F32;
     p.epi.out[0] = w.partials;
     p.epi.out_ld = dk;
@@ -141,6 +174,7 @@ int linattn_forward(const LinArgs& a, const LinDims& D, int* status, unsigned lo
     Problem p = prob0(b, dv, dk, BH * nc, 1, bn);
     p.a[0] = LB.op(Tq, 0, 0, b, BM);
     p.b[0] = LB.op(TS, 0, 0, dv, bn);
+    p.kd = (tc && dk % 128 == 0) ? 2 : 1;   // one 128-deep stage per tile for dk = 128
     p.epi.kind = EPI_OUT;
     p.epi.out[0] = a.out;
     p.epi.out_ld = dv;

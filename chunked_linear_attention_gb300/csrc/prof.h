@@ -22,6 +22,7 @@ enum ProfTag : int {
   PT_MUON,
   PT_MUON_PANEL,
   PT_MUON_HALF,
+  PT_LIN_FUSED,
   PT_COUNT
 };
 

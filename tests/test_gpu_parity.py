@@ -195,6 +195,7 @@ LIN_CASES = [
     dict(mode=W.BIDIRECTIONAL, chunk=1024, N=1024),
     dict(mode=W.STRIDED, chunk=128, N=1024, update_chunks=(0, 1, 1, 0, 1, 0, 0, 1)),
     dict(mode=W.BLOCK_CAUSAL, chunk=256, N=768, d_k=64, d_v=192),
+    dict(mode=W.APPLY_THEN_UPDATE, chunk=512, N=2048, d_k=64, d_v=128),
 ]
 
 
@@ -367,3 +368,22 @@ def test_layer_host_buffers_match_device_call(case):
         assert torch.equal(g_, r_)
     if case["momentum"]:
         assert torch.equal(hmom, dmom.cpu())
+
+
+def test_linattn_output_16_byte_aligned():
+    """An output buffer that is 16- but not 32-byte aligned takes the
+    multi-launch path instead of the one-launch kernel; both match the oracle."""
+    cla = lib()
+    wl = dataclasses.replace(W.LINATTN_C2, B=2, H=2, N=1024, chunk=256)
+    q, k, v, eta, S0 = W.linattn_inputs(wl, with_state=True)
+    ro, rS = O.linattn_chunked_forward(f64(q), f64(k), f64(v), f64(eta), f64(S0), wl.chunk,
+                                       wl.mode, wl.update_chunks)
+    for shift in (0, 8):
+        buf = torch.empty(q.numel() + 16, dtype=torch.bfloat16, device=DEV)
+        out = buf[shift:shift + q.numel()].view(q.shape)
+        o, S = cla.linattn_chunked_forward(q.to(DEV), k.to(DEV), v.to(DEV), eta.to(DEV),
+                                           wl.chunk, wl.mode, S0=S0.to(DEV), out=out)
+        torch.cuda.synchronize()
+        assert_status_ok(cla)
+        assert rel_l2(f64(o), ro) <= BF16_REL_L2
+        assert rel_l2(f64(S), rS) <= BF16_REL_L2
