@@ -200,6 +200,51 @@ __device__ __forceinline__ float grad_block(const EpiDesc& e, float (&v0)[16], c
   return sumsq;
 }
 
+// Gradient epilogue with momentum on the lane-per-row path, for a warp slice
+// of at most four 16-column blocks: the old momentum of every block is loaded
+// before the accumulator wait, so the loads overlap the main loop (a tile's
+// 2048-deep K loop takes ~20 us) instead of following it one block at a time.
+__device__ __forceinline__ float grad_blocks_prefetched(const Problem& P, int tn, uint32_t tl,
+                                                        int c_begin, int c_end,
+                                                        long long tile_base, int rows_valid,
+                                                        uint32_t st, int lane, uint64_t* accf,
+                                                        uint32_t accf_parity, int* status,
+                                                        unsigned long long lim, bool* ok_out) {
+  const EpiDesc& e = P.epi;
+  const int bn = P.bn;
+  float m[4][16];
+#pragma unroll
+  for (int bi = 0; bi < 4; ++bi) {
+    const int c0 = c_begin + 16 * bi;
+    const int gcol = tn * bn + c0;
+    BlockIn<float, 16> g;
+    if (c0 < c_end && rows_valid > 0 && gcol < P.N) {
+      block_fetch<float, 16, true>(e.mom + tile_base + gcol, e.out_ld, rows_valid, g, lane);
+    } else {
+#pragma unroll
+      for (int u = 0; u < BlockIn<float, 16>::kU; ++u) g.w[u] = make_uint4(0, 0, 0, 0);
+    }
+    block_to_row<float, 16, true>(g, st, m[bi], lane);
+  }
+  const bool ok = mbar_wait(accf, accf_parity, status, lim);
+  *ok_out = ok;
+  tc_fence_after();
+  float sumsq = 0.f;
+  if (!ok) return sumsq;
+#pragma unroll
+  for (int bi = 0; bi < 4; ++bi) {
+    const int c0 = c_begin + 16 * bi;
+    if (c0 >= c_end) break;
+    float v0[16];
+    tmem_load_block<16>(tl + c0, v0);
+    tmem_wait_block<16>(v0);
+    const int gcol = tn * bn + c0;
+    if (rows_valid <= 0 || gcol >= P.N) continue;
+    sumsq += grad_block<true>(e, v0, m[bi], tile_base + gcol, rows_valid, st, lane);
+  }
+  return sumsq;
+}
+
 // Blocks of one tile for one epilogue kind (the kind is uniform per tile, so
 // each kind is its own non-inlined loop and keeps only the registers it needs).
 // V8: every row the problem touches is 32-byte aligned (decided on the host).
@@ -221,6 +266,11 @@ __device__ __noinline__ float tc_epilogue_blocks(const Problem& P, int tn, uint3
   const bool has_mom = kInF32 && e.mom != nullptr;
   // the polynomial product may take G from the other TMEM accumulator buffer
   const bool x_tmem = KIND == EPI_NS_POLY && e.in_tmem;
+  if constexpr (KIND == EPI_GRAD && V8 && BW == 16) {
+    if (has_mom && c_end - c_begin <= 64)
+      return grad_blocks_prefetched(P, tn, tl, c_begin, c_end, tile_base, rows_valid, st, lane,
+                                    accf, accf_parity, status, lim, ok_out);
+  }
   BlockIn<__nv_bfloat16, BW> gin16;
   BlockIn<float, BW> gin32;
   auto prefetch = [&](int c0) {
