@@ -9,28 +9,80 @@
 
 namespace ttt {
 
-// ------------------------------------------------------------ init weights
-__global__ void init_weights_kernel(const float* __restrict__ init, int init_per_batch,
-                                    float* __restrict__ master, __nv_bfloat16* __restrict__ work,
-                                    int H, long long per_mat, long long total) {
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    const long long bh = i / per_mat, e = i - bh * per_mat;
-    const long long src = (init_per_batch ? bh : bh % H) * per_mat + e;
-    const float w = init[src];
-    master[i] = w;
-    if (work) work[i] = __float2bfloat16_rn(w);
+// ------------------------------------------------------------ init
+// All of a layer call's state setup in one launch: for each of up to three
+// weight sets, master = init (broadcast over the batch unless per batch) and
+// work = bf16(master); then `nz` floats at `zero` are cleared (momentum,
+// squared-norm partials).  Four elements per thread step when every matrix
+// size is a multiple of 4 (then all rows are 16-byte aligned).
+struct InitArgs {
+  MatSet sets[3];
+  int nsets, B, H, vec4;
+  float* zero[2];
+  long long nz[2];
+};
+
+__global__ void __launch_bounds__(256) init_layer_kernel(const __grid_constant__ InitArgs a) {
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long nthreads = (long long)gridDim.x * blockDim.x;
+  const int BH = a.B * a.H;
+  for (int s = 0; s < a.nsets; ++s) {
+    const MatSet& m = a.sets[s];
+    const long long per = (long long)m.rows * m.cols;
+    __nv_bfloat16* work = static_cast<__nv_bfloat16*>(m.work);
+    if (a.vec4) {
+      const long long per4 = per / 4, n4 = per4 * BH;
+      for (long long i = tid; i < n4; i += nthreads) {
+        const long long bh = i / per4, e = i - bh * per4;
+        const long long src = (m.init_per_batch ? bh : bh % a.H) * per4 + e;
+        const float4 w = reinterpret_cast<const float4*>(m.init)[src];
+        reinterpret_cast<float4*>(m.master)[i] = w;
+        if (work) {
+          __nv_bfloat162 lo = __floats2bfloat162_rn(w.x, w.y), hi = __floats2bfloat162_rn(w.z, w.w);
+          uint2 u;
+          u.x = *reinterpret_cast<uint32_t*>(&lo);
+          u.y = *reinterpret_cast<uint32_t*>(&hi);
+          reinterpret_cast<uint2*>(work)[i] = u;
+        }
+      }
+    } else {
+      const long long n = per * BH;
+      for (long long i = tid; i < n; i += nthreads) {
+        const long long bh = i / per, e = i - bh * per;
+        const float w = m.init[(m.init_per_batch ? bh : bh % a.H) * per + e];
+        m.master[i] = w;
+        if (work) work[i] = __float2bfloat16_rn(w);
+      }
+    }
   }
+  for (int z = 0; z < 2; ++z)
+    for (long long i = tid; i < a.nz[z]; i += nthreads) a.zero[z][i] = 0.f;
 }
 
-cudaError_t launch_init_weights(const MatSet& m, int B, int H, cudaStream_t stream) {
-  const long long per = (long long)m.rows * m.cols;
-  const long long total = per * B * H;
-  const int threads = 256;
-  long long blocks = (total + threads - 1) / threads;
-  if (blocks > 152 * 16) blocks = 152 * 16;
-  init_weights_kernel<<<(int)blocks, threads, 0, stream>>>(
-      m.init, m.init_per_batch, m.master, static_cast<__nv_bfloat16*>(m.work), H, per, total);
+cudaError_t launch_init_layer(const MatSet* sets, int nsets, int B, int H, float* zero0,
+                              long long n0, float* zero1, long long n1, cudaStream_t stream) {
+  InitArgs a{};
+  a.nsets = nsets;
+  a.B = B;
+  a.H = H;
+  a.vec4 = 1;
+  long long most = 0;
+  for (int s = 0; s < nsets; ++s) {
+    a.sets[s] = sets[s];
+    const long long per = (long long)sets[s].rows * sets[s].cols;
+    if (per % 4 != 0) a.vec4 = 0;
+    most = per * B * H > most ? per * B * H : most;
+  }
+  a.zero[0] = zero0;
+  a.nz[0] = zero0 ? n0 : 0;
+  a.zero[1] = zero1;
+  a.nz[1] = zero1 ? n1 : 0;
+  most = a.vec4 ? most / 4 : most;
+  most = most > a.nz[0] ? most : a.nz[0];
+  most = most > a.nz[1] ? most : a.nz[1];
+  long long blocks = (most + 255) / 256;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  init_layer_kernel<<<(int)(blocks > 0 ? blocks : 1), 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

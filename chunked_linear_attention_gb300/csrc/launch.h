@@ -29,8 +29,11 @@ struct MatSet {
   int rows, cols;
 };
 
-// master = init (broadcast over the batch), work = bf16(master).
-cudaError_t launch_init_weights(const MatSet& m, int B, int H, cudaStream_t stream);
+// For up to three sets in one launch: master = init (broadcast over the batch
+// unless per batch), work = bf16(master); also clears n0 floats at zero0 and
+// n1 at zero1 (either may be NULL).
+cudaError_t launch_init_layer(const MatSet* sets, int nsets, int B, int H, float* zero0,
+                              long long n0, float* zero1, long long n1, cudaStream_t stream);
 
 // master = RowNorm(master - update) (or master - update), work = bf16(master).
 cudaError_t launch_update_normalize(const MatSet* sets, int nsets, int BH, int l2norm,

@@ -482,9 +482,11 @@ bool stagger_on() {
 
 // Number of stream groups the (batch, head) sequences are split into: each
 // group's launches cover a contiguous range of sequences on its own stream.
-// The default is two groups (measured best on the 760M-scale layer, B*H = 8,
-// among 1, 2, 4 and 8); TTT_SEQUENCE_GROUPS (1 .. B*H) overrides it, and 1
-// runs every launch batched over all sequences on the caller's stream.
+// The default is three groups (measured best on the 760M-scale layer, B*H = 8,
+// among 1 to 6: 4.41, 3.27, 3.19, 3.25, 3.26, 3.29 ms per step; smaller
+// Newton-Schulz launches pack better between the other groups' GEMMs);
+// TTT_SEQUENCE_GROUPS (1 .. B*H) overrides it, and 1 runs every launch batched
+// over all sequences on the caller's stream.
 int sequence_groups(const LayerDims& D) {
   const int BH = D.B * D.H;
   if (!per_sequence_streams(D)) return 1;
@@ -494,7 +496,7 @@ int sequence_groups(const LayerDims& D) {
     env = (s && s[0]) ? std::atoi(s) : -1;
   }
   if (env >= 1) return env < BH ? env : BH;
-  return 2;
+  return BH < 3 ? BH : 3;
 }
 
 // Host-buffer calls: chunks [c, c + n) of q, k, v and eta for every
@@ -530,7 +532,6 @@ int enqueue_all(LayerPlan& L, cudaStream_t st) {
   const int BH = D.B * D.H;
   const int nc = D.N / D.chunk;
   const long long dm = (long long)D.d * D.m;
-  const int rows_of[3] = {D.m, D.m, D.d}, cols_of[3] = {D.d, D.d, D.m};
 
   // streams: [0, ng) compute groups when ng > 1; host-buffer calls add one
   // host-to-device stream and one device-to-host stream per group
@@ -576,18 +577,15 @@ int enqueue_all(LayerPlan& L, cudaStream_t st) {
       hooks[g] = IoHooks{chunk_ev.data(), nc, io[1 + g], evs[nb + g]};
   }
 
-  for (int s = 0; s < 3; ++s) {
-    ProfScope ps(PT_INIT, st, 0.0,
-                 (double)BH * rows_of[s] * cols_of[s] * (4 + 4 + (tc ? 2 : 0)));
-    TTT_CK(launch_init_weights(L.ms[s], D.B, D.H, st));
-  }
-  if (!a.momentum && w.M) {
-    ProfScope ps(PT_INIT, st, 0.0, 3.0 * BH * dm * 4);
-    TTT_CK(launch_copy_f32(w.M, nullptr, 3LL * BH * dm, st));
-  }
   {
-    ProfScope ps(PT_INIT, st, 0.0, 3.0 * BH * 4);
-    TTT_CK(launch_copy_f32(w.normsq, nullptr, 3LL * BH * (1 + w.nslot), st));
+    // weights and their bf16 copies, a zero momentum (when none is passed) and
+    // the squared-norm partials, in one launch
+    float* mz = (!a.momentum && w.M) ? w.M : nullptr;
+    ProfScope ps(PT_INIT, st, 0.0,
+                 3.0 * BH * dm * (4 + 4 + (tc ? 2 : 0)) + (mz ? 3.0 * BH * dm * 4 : 0.0) +
+                     3.0 * BH * (1 + w.nslot) * 4);
+    TTT_CK(launch_init_layer(L.ms, 3, D.B, D.H, mz, 3LL * BH * dm, w.normsq,
+                             3LL * BH * (1 + w.nslot), st));
   }
   MapCache cache;
   if (ng > 1) {

@@ -26,7 +26,7 @@ const char* kTagName[PT_COUNT] = {
     "norm", "lin.scale", "gemm.lin_partial", "lin.prefix", "gemm.lin_out", "gemm.selftest", "muon.cluster",
     "muon.panel", "muon.half", "lin.fused"};
 const char* kTagKernel[PT_COUNT] = {
-    "init_weights_kernel", "umma_gemm_kernel", "umma_gemm_kernel", "umma_gemm_kernel",
+    "init_layer_kernel", "umma_gemm_kernel", "umma_gemm_kernel", "umma_gemm_kernel",
     "umma_gemm_kernel", "umma_gemm_kernel", "update_normalize_kernel", "scale_rows_kernel",
     "umma_gemm_kernel", "linattn_prefix_kernel", "umma_gemm_kernel", "umma_gemm_kernel",
     "ns_cluster_kernel", "ns_panel_kernel", "ns_half_kernel", "linattn_fused_kernel"};
