@@ -103,6 +103,7 @@ OpDesc LaunchBuilder::op(const TensorRef& t, int mn_major, int outer_base, int z
                          int box_rows, int mn_krows) {
   OpDesc o;
   std::memset(&o, 0, sizeof(o));
+  o.map3 = -1;
   o.mn_major = mn_major;
   o.outer_base = outer_base;
   o.inner_base = 0;
@@ -121,7 +122,7 @@ OpDesc LaunchBuilder::op(const TensorRef& t, int mn_major, int outer_base, int z
     int slot = -1;
     for (int i = 0; i < nmaps_; ++i)
       if (keys_ptr_[i] == t.ptr && keys_rows_[i] == t.rows && keys_inner_[i] == t.inner &&
-          keys_box_[i] == box)
+          keys_box_[i] == box && keys_nblk_[i] == 0)
         slot = i;
     if (slot < 0) {
       if (nmaps_ >= kMaxMaps || !cache_->get(t, box, &L_.maps[nmaps_])) {
@@ -133,8 +134,10 @@ OpDesc LaunchBuilder::op(const TensorRef& t, int mn_major, int outer_base, int z
       keys_rows_[slot] = t.rows;
       keys_inner_[slot] = t.inner;
       keys_box_[slot] = box;
+      keys_nblk_[slot] = 0;
     }
     o.map = slot;
+    o.map3 = -1;
   }
   return o;
 }
@@ -166,6 +169,26 @@ static bool epi_rows32(const EpiDesc& e) {
   return true;
 }
 
+int LaunchBuilder::blocked_slot(int map2d, int cols) {
+  if (map2d < 0 || cols < 128 || cols % 64 != 0 || keys_inner_[map2d] % 64 != 0) return -1;
+  const int nblk = cols / 64;
+  for (int i = 0; i < nmaps_; ++i)
+    if (keys_ptr_[i] == keys_ptr_[map2d] && keys_rows_[i] == keys_rows_[map2d] &&
+        keys_inner_[i] == keys_inner_[map2d] && keys_box_[i] == keys_box_[map2d] &&
+        keys_nblk_[i] == nblk)
+      return i;
+  if (nmaps_ >= kMaxMaps) return -1;
+  const TensorRef t{keys_ptr_[map2d], 1, keys_rows_[map2d], keys_inner_[map2d]};
+  if (!cache_->get_blocked(t, keys_box_[map2d], nblk, &L_.maps[nmaps_])) return -1;
+  const int slot = nmaps_++;
+  keys_ptr_[slot] = t.ptr;
+  keys_rows_[slot] = t.rows;
+  keys_inner_[slot] = t.inner;
+  keys_box_[slot] = keys_box_[map2d];
+  keys_nblk_[slot] = nblk;
+  return slot;
+}
+
 bool LaunchBuilder::add(Problem p) {
   if (L_.nprob >= kMaxProblems) {
     ok_ = false;
@@ -184,6 +207,16 @@ bool LaunchBuilder::add(Problem p) {
     }
   }
   if (!tc_) p.kd = 1;
+  if (tc_) {
+    // MN-major tiles of two or more 64-column blocks: one 3-D box per stage
+    // instead of one box per block (fewer, larger TMA transfers)
+    for (int j = 0; j < p.nacc; ++j) {
+      if (p.a[j].mn_major && p.a[j].inner_base % 64 == 0)
+        p.a[j].map3 = blocked_slot(p.a[j].map, bm());
+      if (p.b[j].mn_major && p.b[j].inner_base % 64 == 0)
+        p.b[j].map3 = blocked_slot(p.b[j].map, p.bn);
+    }
+  }
   const int bm = this->bm();
   if (!tc_) p.bn = kSimtTile;
   p.tiles_m = (p.M + bm - 1) / bm;

@@ -74,6 +74,10 @@ class LaunchBuilder {
   long long keys_rows_[kMaxMaps];
   int keys_inner_[kMaxMaps];
   int keys_box_[kMaxMaps];
+  int keys_nblk_[kMaxMaps];   // 0: 2-D map; else a 3-D blocked map of nblk 64-column blocks
+  // Slot of the 3-D blocked map for an MN-major operand whose tile spans
+  // `cols` columns (>= 128), or -1 when the 2-D boxes must serve.
+  int blocked_slot(int map2d, int cols);
   bool ok_;
   int* status_;
   unsigned long long wait_ns_;

@@ -16,7 +16,7 @@
 namespace ttt {
 
 constexpr int kMaxProblems = 4;
-constexpr int kMaxMaps = 10;
+constexpr int kMaxMaps = 14;
 constexpr int kMaxAcc = 3;
 
 enum EpiKind : int {
@@ -33,7 +33,9 @@ enum EpiKind : int {
 // One operand of one accumulator.
 struct OpDesc {
   // tensor-core path: a 2-D TMA map over the backing tensor
-  int map;            // slot in GemmLaunch::maps
+  short map;          // slot in GemmLaunch::maps
+  short map3;         // MN-major tiles of 128+ columns: a 3-D map whose one box is the
+                      // whole stage tile (64-column blocks), or -1 (one box per block)
   int mn_major;       // 0: K contiguous; 1: M/N contiguous
   int outer_base;     // outer (row) coordinate of batch 0's origin
   int inner_base;     // inner (column) coordinate of batch 0's origin

@@ -117,6 +117,7 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int mn_major, in
 // are 128 K rows deep (`bbytes` = 16 KB apart instead of 8 KB).
 struct OpCoords {
   const CUtensorMap* map;
+  const CUtensorMap* map3;   // MN-major: the whole stage tile as one 3-D box, or NULL
   int x0, y0, dx, dy, nbox, kd, kbytes, bbytes;
 };
 
@@ -125,6 +126,7 @@ __device__ __forceinline__ OpCoords op_coords(const CUtensorMap* maps, const OpD
   const int zz = op.z_div > 1 ? z / op.z_div : z;
   OpCoords c;
   c.map = &maps[op.map];
+  c.map3 = (op.mn_major && op.map3 >= 0) ? &maps[op.map3] : nullptr;
   c.kd = kd;
   c.kbytes = rows * kBK * 2;
   c.bbytes = 8192 * kd;
@@ -149,6 +151,8 @@ __device__ __forceinline__ void issue_op(const OpCoords& c, uint8_t* dst, int ks
   if (c.dy == 0) {   // K-major: kd boxes of 64 K columns
     tma_load_2d(dst, c.map, x, y, bar);
     if (c.kd == 2) tma_load_2d(dst + c.kbytes, c.map, x + kBK, y, bar);
+  } else if (c.map3) {   // blocks of 64 columns land c.bbytes apart, as below
+    tma_load_3d(dst, c.map3, 0, y, x >> 6, bar);
   } else {
     for (int i = 0; i < c.nbox; ++i) tma_load_2d(dst + i * c.bbytes, c.map, x + i * 64, y, bar);
   }
