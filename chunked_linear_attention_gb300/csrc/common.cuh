@@ -403,6 +403,17 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start (its prologue) before the previous kernel in the
+// stream has finished; pdl_wait() blocks until that kernel has completed and
+// its memory operations are visible, and must precede every access to memory
+// the previous kernels wrote or read.  pdl_launch_dependents() lets the next
+// such kernel start once every CTA of this grid has issued it (or exited).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Orders this thread's generic-proxy global writes before later async-proxy
 // (TMA) reads of the same addresses.
 __device__ __forceinline__ void fence_proxy_async_global() {

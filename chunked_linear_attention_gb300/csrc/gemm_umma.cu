@@ -92,6 +92,9 @@ __global__ void __launch_bounds__(kGemmKernelThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const unsigned long long lim = L.wait_limit_ns;
+  // everything above is this launch's own setup; from here on it reads and
+  // writes what earlier launches in the stream produced or still read
+  pdl_wait();
 
   if (warp == 0 || warp == 2) {
     // Two producer threads in different warps share the ring entries round
@@ -129,6 +132,9 @@ __global__ void __launch_bounds__(kGemmKernelThreads, 1)
         umma_commit(&accf[buf]);
         if (!ok) break;
       }
+      // the main loops are done: the next launch may start its setup while the
+      // epilogues finish
+      pdl_launch_dependents();
     }
   } else {
     int it = 0;
@@ -196,13 +202,21 @@ cudaError_t launch_umma_gemm(const GemmLaunch& L, cudaStream_t stream) {
   const int* sm_count = g_sm_count;
   if (L.total_tiles <= 0) return cudaSuccess;
   const int grid = L.total_tiles < sm_count[dev] ? L.total_tiles : sm_count[dev];
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kGemmKernelThreads, 1, 1);
+  cfg.dynamicSmemBytes = kUmmaSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   bool rows32 = true;
   for (int p = 0; p < L.nprob; ++p) rows32 = rows32 && L.prob[p].epi.rows32;
   if (rows32)
-    umma_gemm_kernel<true><<<grid, kGemmKernelThreads, kUmmaSmemBytes, stream>>>(L);
-  else
-    umma_gemm_kernel<false><<<grid, kGemmKernelThreads, kUmmaSmemBytes, stream>>>(L);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, umma_gemm_kernel<true>, L);
+  return cudaLaunchKernelEx(&cfg, umma_gemm_kernel<false>, L);
 }
 
 }  // namespace ttt

@@ -255,10 +255,6 @@ __global__ void __launch_bounds__(kHThreads, 1)
   const int mrow = z * d;                     // first row of this matrix in the stacked buffers
   const int prow = mrow + r * 128;            // first row of this CTA's panel
   const unsigned long long lim = L.wait_limit_ns;
-  // every warp sums the partials in the same fixed order (same value everywhere)
-  const float s1 =
-      1.0f / (sqrtf(sum_partials_warp(L.normsq_part + (long long)z * L.nslot, L.nslot)) + L.eps);
-
   if (threadIdx.x == 0) {
     for (int s = 0; s < nstages; ++s) {
       mbar_init(&full[s], 1);
@@ -279,6 +275,12 @@ __global__ void __launch_bounds__(kHThreads, 1)
   cluster_sync_all();   // peers signal our barriers: initialise them first
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the setup above touches no global memory; the gradient launch before this
+  // one in the stream wrote the iterates and the norm partials read below
+  pdl_wait();
+  // every warp sums the partials in the same fixed order (same value everywhere)
+  const float s1 =
+      1.0f / (sqrtf(sum_partials_warp(L.normsq_part + (long long)z * L.nslot, L.nslot)) + L.eps);
   const uint32_t peer_pready = map_cluster(smem_u32(pready), (uint32_t)partner);
   const uint32_t peer_panel = map_cluster(smem_u32(apanel), (uint32_t)partner);
   const uint32_t peer_rs = map_cluster(smem_u32(rs_peer), (uint32_t)partner);
@@ -467,6 +469,10 @@ __global__ void __launch_bounds__(kHThreads, 1)
     }
   }
 
+  // the last product's MMAs are issued: the next launch may start its setup
+  // while the update finishes
+  if (warp == 1 && lane == 0) pdl_launch_dependents();
+
   // every peer's multicast commit into our ring barriers must have landed
   if (warp == 0 && lane == 0 && ok) {
     const int n = issued < nstages ? issued : nstages;
@@ -571,17 +577,19 @@ int launch_ns_half(MapCache& cache, const NsArgs& a, int* status, unsigned long 
   L.wait_limit_ns = wait_ns;
 
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(3 * a.nh * cs, 1, 1);
   cfg.blockDim = dim3(kHThreads, 1, 1);
   cfg.dynamicSmemBytes = kUmmaSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   const double n3 = (double)d * d * d;
   const double flops = 3.0 * a.nh * a.steps * 6.0 * n3;
   ProfScope ps(PT_MUON_HALF, stream, flops, 0.0);
