@@ -241,12 +241,27 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 
-// Bounded cluster-scope wait (as mbar_wait).
+__device__ __forceinline__ bool mbar_try_wait_cluster_sleep(uint64_t* bar, uint32_t parity,
+                                                            uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded cluster-scope wait (as mbar_wait: the waiting thread stays suspended
+// in the try_wait instead of spinning on the clock).
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int* status,
                                                   unsigned long long limit_ns) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
   unsigned long long t0 = 0;
   for (;;) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (mbar_try_wait_cluster_sleep(bar, parity, 1000000u)) return true;
     const unsigned long long now = global_ns();
     if (t0 == 0) {
       t0 = now;
