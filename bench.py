@@ -301,12 +301,19 @@ def roofline_entry(name, agg, peak, peak_src):
     fl = agg["flops"] / n
     achieved = fl / (avg_ms / 1e3) / 1e12 if avg_ms > 0 else None
     traffic, src = recorded_traffic(name)
+    share = agg["sm_ms"] / agg["ms"] if agg.get("ms") else None
     return {"bound": "tensor", "kernel": name, "achieved": achieved, "peak": peak,
             "unit": "TFLOP/s", "frac": achieved / peak if achieved and peak else None,
             "peak_kind": f"bf16 sustained ({peak_src}): the kernel runs inside a long step",
             "traffic": traffic, "traffic_unit": "bytes per launch (ncu dram read + write)",
             "traffic_source": src, "launches_per_step": agg["launches"],
-            "flops_per_launch": fl, "avg_launch_us": avg_ms * 1e3}
+            "flops_per_launch": fl, "avg_launch_us": avg_ms * 1e3,
+            "dominance": "most GPU time: device time x fraction of SMs the grid holds",
+            "gpu_ms_per_step": agg.get("sm_ms"), "avg_sm_share": share,
+            "achieved_on_held_sms": (agg["flops"] / (agg["sm_ms"] / 1e3) / 1e12
+                                     if agg.get("sm_ms") else None),
+            "achieved_on_held_sms_note": "FLOPs over device time x SM share: the rate on the "
+                                         "SMs the launches hold, scaled to the whole GPU"}
 
 
 def time_steps(torch, fn, steps, warmup, stream):
@@ -404,14 +411,19 @@ def run_ours(args):
     gemm = [p for p in prof if p["kernel"] in tc_kernels]
     g_fl = sum(p["flops"] for p in gemm)
     g_n = sum(p["launches"] for p in gemm)
-    # the dominant kernel: most device time in the profiled step
+    # The dominant kernel: most GPU time in the profiled step, counted as each
+    # launch's device time x the fraction of the SMs its grid holds (launches
+    # of the stream groups and the apply streams run side by side, several of
+    # them on a part of the GPU).
     per_kernel = {}
     for p in gemm:
-        k_ = per_kernel.setdefault(p["kernel"], {"launches": 0, "ms": 0.0, "flops": 0.0})
+        k_ = per_kernel.setdefault(p["kernel"], {"launches": 0, "ms": 0.0, "flops": 0.0,
+                                                 "sm_ms": 0.0})
         k_["launches"] += p["launches"]
         k_["ms"] += p["ms"]
         k_["flops"] += p["flops"]
-    dom_name, dom = max(per_kernel.items(), key=lambda kv: kv[1]["ms"])
+        k_["sm_ms"] += p.get("sm_ms", p["ms"])
+    dom_name, dom = max(per_kernel.items(), key=lambda kv: kv[1]["sm_ms"])
     peaks, peak_src = load_peaks()
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -487,6 +499,7 @@ def run_ours(args):
             "breakdown_note": "summed launch durations of one profiled step; launches of "
                               "different sequences overlap, so sums exceed the step time",
             "breakdown": {p["name"]: {"launches": p["launches"], "ms": p["ms"],
+                                      "gpu_ms": p.get("sm_ms"),
                                       "tflops": p["flops"] / (p["ms"] / 1e3) / 1e12
                                       if p["flops"] and p["ms"] else None,
                                       "gbs": p["bytes"] / (p["ms"] / 1e3) / 1e9

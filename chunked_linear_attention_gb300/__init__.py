@@ -41,7 +41,8 @@ class ProfileEntry(ctypes.Structure):
     """Mirror of ``ttt_profile_entry``."""
     _fields_ = [("name", ctypes.c_char * 32), ("kernel", ctypes.c_char * 32),
                 ("launches", ctypes.c_int), ("ms", ctypes.c_double),
-                ("flops", ctypes.c_double), ("bytes", ctypes.c_double)]
+                ("flops", ctypes.c_double), ("bytes", ctypes.c_double),
+                ("sm_ms", ctypes.c_double)]
 
 
 class UpdateRule(ctypes.Structure):
@@ -342,13 +343,13 @@ def profile_start():
 
 
 def profile_stop():
-    """Per launch kind: dict(name, kernel, launches, ms, flops, bytes)."""
+    """Per launch kind: dict(name, kernel, launches, ms, flops, bytes, sm_ms)."""
     arr = (ProfileEntry * 32)()
     n = library().ttt_profile_stop(arr, 32)
     if n < 0:
         raise TTTError(n, "ttt_profile_stop")
     return [dict(name=e.name.decode(), kernel=e.kernel.decode(), launches=e.launches, ms=e.ms,
-                 flops=e.flops, bytes=e.bytes) for e in arr[:n]]
+                 flops=e.flops, bytes=e.bytes, sm_ms=e.sm_ms) for e in arr[:n]]
 
 
 def set_wait_limit_ns(ns: int):

@@ -227,7 +227,7 @@ bool LaunchBuilder::add(Problem p) {
   return true;
 }
 
-cudaError_t LaunchBuilder::launch(cudaStream_t stream, int tag) {
+cudaError_t LaunchBuilder::launch(cudaStream_t stream, int tag, int priority, int max_ctas) {
   if (!ok_) return cudaErrorInvalidValue;
   double flops = 0;
   for (int i = 0; i < L_.nprob; ++i) {
@@ -236,8 +236,10 @@ cudaError_t LaunchBuilder::launch(cudaStream_t stream, int tag) {
   }
   cudaError_t e;
   {
-    ProfScope ps(tag, stream, flops, 0.0);
-    e = tc_ ? launch_umma_gemm(L_, stream) : launch_simt_gemm(L_, stream);
+    const int sms = tc_ ? device_sm_count() : 0;
+    const double share = sms > 0 ? (double)umma_gemm_grid(L_, max_ctas) / sms : 1.0;
+    ProfScope ps(tag, stream, flops, 0.0, share);
+    e = tc_ ? launch_umma_gemm(L_, stream, priority, max_ctas) : launch_simt_gemm(L_, stream);
   }
   reset();
   return e;

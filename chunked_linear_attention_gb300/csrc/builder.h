@@ -59,8 +59,9 @@ class LaunchBuilder {
   int choose_bn(int N, int nacc) const;
   // Fills tiles and appends.  Returns false when the launch is full.
   bool add(Problem p);
-  // Launches with launch accounting under profile tag `tag`.
-  cudaError_t launch(cudaStream_t stream, int tag);
+  // Launches with launch accounting under profile tag `tag` (tensor-core
+  // launches at `priority`, 0 = the stream's own).
+  cudaError_t launch(cudaStream_t stream, int tag, int priority = 0, int max_ctas = 0);
   bool ok() const { return ok_; }
   bool tensor_cores() const { return tc_; }
   int bm() const { return tc_ ? 128 : kSimtTile; }

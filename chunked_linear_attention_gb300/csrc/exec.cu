@@ -89,6 +89,20 @@ bool stagger_events(int n, std::vector<cudaEvent_t>* out) {
   return true;
 }
 
+int high_priority() {
+  static int cached[kMaxDevices];
+  static bool done[kMaxDevices] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lk(g_pool_mu);
+  if (!done[dev]) {
+    int least = 0, greatest = 0;
+    cached[dev] = cudaDeviceGetStreamPriorityRange(&least, &greatest) == cudaSuccess ? greatest : 0;
+    done[dev] = true;
+  }
+  return cached[dev];
+}
+
 bool io_events(int n, std::vector<cudaEvent_t>* out) {
   if (n > 4096) return false;
   std::lock_guard<std::mutex> lk(g_pool_mu);

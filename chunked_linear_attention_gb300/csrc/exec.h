@@ -30,6 +30,11 @@ bool stagger_events(int n, std::vector<cudaEvent_t>* out);
 // the other pools; n <= 4096).  Returns false on failure.
 bool io_events(int n, std::vector<cudaEvent_t>* out);
 
+// The highest launch priority of the current device (0 when priorities are
+// not supported): launches on the critical path of a call use it so that
+// work off that path only fills the SMs it leaves free.
+int high_priority();
+
 // Runs `enqueue(stream)` through a cached graph when possible: on the first
 // call with a given key the launch sequence is captured on an internal stream
 // and instantiated; every call then launches the graph on `stream`.  Falls

@@ -194,24 +194,38 @@ cudaError_t prepare_umma_gemm() {
   return cudaSuccess;
 }
 
-cudaError_t launch_umma_gemm(const GemmLaunch& L, cudaStream_t stream) {
-  cudaError_t e = prepare_umma_gemm();
-  if (e != cudaSuccess) return e;
+int device_sm_count() {
+  if (prepare_umma_gemm() != cudaSuccess) return 0;
   int dev = 0;
   cudaGetDevice(&dev);
-  const int* sm_count = g_sm_count;
+  return g_sm_count[dev];
+}
+
+int umma_gemm_grid(const GemmLaunch& L, int max_ctas) {
+  const int sms = device_sm_count();
+  int grid = L.total_tiles < sms ? L.total_tiles : sms;
+  if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
+  return grid;
+}
+
+cudaError_t launch_umma_gemm(const GemmLaunch& L, cudaStream_t stream, int priority,
+                             int max_ctas) {
+  cudaError_t e = prepare_umma_gemm();
+  if (e != cudaSuccess) return e;
   if (L.total_tiles <= 0) return cudaSuccess;
-  const int grid = L.total_tiles < sm_count[dev] ? L.total_tiles : sm_count[dev];
+  const int grid = umma_gemm_grid(L, max_ctas);
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributePriority;
+  attr[1].val.priority = priority;
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kGemmKernelThreads, 1, 1);
   cfg.dynamicSmemBytes = kUmmaSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = priority != 0 ? 2 : 1;
   bool rows32 = true;
   for (int p = 0; p < L.nprob; ++p) rows32 = rows32 && L.prob[p].epi.rows32;
   if (rows32)

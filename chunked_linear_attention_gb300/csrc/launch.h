@@ -12,7 +12,17 @@ namespace ttt {
 constexpr int kUmmaSmemBytes = 227 * 1024;
 constexpr int kSimtTile = 64;
 
-cudaError_t launch_umma_gemm(const GemmLaunch& L, cudaStream_t stream);
+// SMs of the current device (0 if unknown).
+int device_sm_count();
+
+// Grid of a tensor-core GEMM launch (the persistent kernel: at most one CTA
+// per SM, capped at `max_ctas` when > 0).
+int umma_gemm_grid(const GemmLaunch& L, int max_ctas);
+
+// `priority`: launch priority (0: the stream's own; lower values run first).
+// `max_ctas` > 0 caps the persistent grid below one CTA per SM.
+cudaError_t launch_umma_gemm(const GemmLaunch& L, cudaStream_t stream, int priority = 0,
+                             int max_ctas = 0);
 // One-time per-device kernel attributes (call before any stream capture).
 cudaError_t prepare_umma_gemm();
 cudaError_t launch_simt_gemm(const GemmLaunch& L, cudaStream_t stream);

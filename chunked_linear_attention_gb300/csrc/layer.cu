@@ -7,14 +7,21 @@
 // weights to one chunk of queries and/or takes one update from one chunk of
 // keys/values, with all (batch, head) pairs batched in every launch:
 //
-//   PROJ  one launch: queries  H1q = Q W1^T, H3q = Q W3^T -> A_q (gated)
-//                     keys     H1 = K W1^T, H3 = K W3^T, VW2 = V W2
+//   APPLY two launches on the apply stream: queries H1q = Q W1^T, H3q = Q W3^T
+//                     -> A_q (gated), then the output O = A_q W2^T of the
+//                     applied chunk (without an apply stream they join the
+//                     PROJ and GRAD launches)
+//   PROJ  one launch: keys     H1 = K W1^T, H3 = K W3^T, VW2 = V W2
 //                              -> dH1, dH3, P (fused SiLU/SiLU' and eta)
 //   GRAD  one launch: g1 = dH1^T K, g3 = dH3^T K, g2 = V^T P (eq 2; K = chunk)
-//                     with momentum fused in the epilogue, and the output
-//                     O = A_q W2^T of the applied chunk
-//   MUON  3 launches per Newton-Schulz step over all matrices (eq 6)
-//   NORM  one launch: W <- L2-Normalize(W - U), refresh bf16 copies (eq 5)
+//                     with momentum fused in the epilogue
+//   MUON  one fused launch (or 3 launches per Newton-Schulz step) over all
+//         matrices (eq 6), ending in W <- L2-Normalize(W - U) (eq 5)
+//   NORM  one launch: W <- L2-Normalize(W - U) without Muon (eq 5)
+//
+// The bf16 operand copies of the weights alternate between two buffers, so
+// that the apply side of one step can still read its weights while the
+// update writes the next ones.
 //
 // Matrix slots: 0 = W1 [m, d], 1 = W3 [m, d], 2 = W2 [d, m]; every
 // per-matrix buffer is [slot][B*H][rows*cols].
@@ -58,6 +65,7 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct LayerWs {
   void* Wb[3];
+  void* Wb2[3];        // second bf16 copy: the apply side reads one while the update writes the other
   void* Aq;
   void* dH1;
   void* dH3;
@@ -91,6 +99,7 @@ size_t layer_ws_layout(const LayerDims& D, LayerWs* w, char* base) {
   LayerWs tmp;
   LayerWs& o = w ? *w : tmp;
   for (int i = 0; i < 3; ++i) o.Wb[i] = D.bf16 ? take(BH * dm * 2) : nullptr;
+  for (int i = 0; i < 3; ++i) o.Wb2[i] = D.bf16 ? take(BH * dm * 2) : nullptr;
   o.Aq = take(BH * D.chunk * D.m * es);
   o.dH1 = take(BH * D.chunk * D.m * es);
   o.dH3 = take(BH * D.chunk * D.m * es);
@@ -155,7 +164,8 @@ struct LayerPlan {
   LayerWs w;
   MatSet ms[3];
   float* mom[3];
-  TensorRef Tq, Tk, Tv, TW[3], TAq, TdH1, TdH3, TP;
+  TensorRef Tq, Tk, Tv, TW[2][3], TAq, TdH1, TdH3, TP;
+  void* wb[2][3];   // the two bf16 copies of the weights (both the first when there is one)
   std::vector<std::pair<int, int>> steps;
   int* status;
   unsigned long long wait_ns;
@@ -177,10 +187,40 @@ struct IoHooks {
   cudaEvent_t out_ev;
 };
 
+// CTAs of each apply-side launch for `nh` sequences (TTT_APPLY_CTAS sets the
+// CTAs per sequence): the persistent GEMM keeps its CTAs for the whole launch,
+// so the apply side is held to a share of the SMs and the update chain finds
+// the rest free.  Measured on the 760M-scale layer (four groups of two
+// sequences): 2, 3, 4, 6 CTAs per sequence -> 3.04, 2.90, 2.93, 2.95 ms per
+// step; uncapped (152 CTAs) 3.2 ms, and 3.11 ms without the split.
+int apply_ctas(int nh) {
+  static int v = -1;
+  if (v < 0) {
+    const char* s = std::getenv("TTT_APPLY_CTAS");
+    v = (s && s[0]) ? std::atoi(s) : 3;
+    if (v < 0) v = 0;
+  }
+  return v * nh;
+}
+
+// The apply side of a step (query projections and the output GEMM of its
+// apply chunk) depends only on that step's weights, and nothing in the scan
+// depends on it.  With an apply stream `sa` it runs there, overlapping the
+// update chain on `st` (projections of the keys, gradients, Newton-Schulz):
+// the update writes the next weights' bf16 copy into the other of the two
+// copies, and waits only until the applies that read that copy (one update
+// earlier) have finished.  ApplyEvents: ev_w is recorded on `st` whenever new
+// weights are complete; ev_a[c] on `sa` after the latest apply that read copy c.
+struct ApplyEvents {
+  cudaEvent_t ev_w;
+  cudaEvent_t ev_a[2];
+};
+
 // `after_first`: if set, recorded on `st` once the first step's projection and
 // gradient launches are enqueued (stream groups start staggered on it).
 int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStream_t st,
-                  cudaEvent_t after_first = nullptr, const IoHooks* io = nullptr) {
+                  cudaEvent_t after_first = nullptr, const IoHooks* io = nullptr,
+                  cudaStream_t sa = nullptr, const ApplyEvents* aev = nullptr) {
   const LayerArgs& a = *L.a;
   const LayerDims& D = *L.D;
   const LayerWs& w = L.w;
@@ -197,24 +237,93 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
   LaunchBuilder LB(tc, &cache, L.status, L.wait_ns);
   const int BM = LB.bm();
   const long long bm_h = (long long)b * m;   // activation elements per (batch, head)
+  const bool split = sa != nullptr && aev != nullptr;
+  // the update chain's launches go first; the apply side fills the SMs they leave
+  const int prio = split ? high_priority() : 0;
+  int cur = 0;                           // bf16 copy holding the current weights
+  bool apply_reads[2] = {false, false};  // an apply that st has not waited for reads copy c
 
-  int waited = -1;   // host-buffer calls: last input chunk this stream waited for
+  if (split) {   // the apply stream starts from everything enqueued on st so far
+    TTT_CK(cudaEventRecord(aev->ev_w, st));
+    TTT_CK(cudaStreamWaitEvent(sa, aev->ev_w, 0));
+  }
+
+  // query projections of chunk ap, appended to the launch being built
+  auto add_apply_proj = [&](int ap) {
+    const int bn = LB.choose_bn(m, 2);
+    Problem p = prob0(b, m, d, nh, 2, bn);
+    p.a[0] = LB.op(L.Tq, 0, h0 * N + ap * b, N, BM);
+    p.b[0] = LB.op(L.TW[cur][0], 0, h0 * m, m, bn);
+    p.a[1] = p.a[0];
+    p.b[1] = LB.op(L.TW[cur][1], 0, h0 * m, m, bn);
+    p.a_shared = 1 << 1;
+    p.epi.kind = EPI_PROJ_Q;
+    p.epi.out[0] = offs(w.Aq, h0 * bm_h);
+    p.epi.out_ld = m;
+    p.epi.out_z = bm_h;
+    LB.add(p);
+  };
+  // output O = A_q W2^T of chunk ap, appended to the launch being built
+  auto add_apply_out = [&](int ap) {
+    const int bn = LB.choose_bn(d, 1);
+    Problem p = prob0(b, d, m, nh, 1, bn);
+    p.a[0] = LB.op(L.TAq, 0, h0 * b, b, BM);
+    p.b[0] = LB.op(L.TW[cur][2], 0, h0 * d, d, bn);  // W2 [d, m]: N = d rows, K = m contiguous
+    p.kd = (tc && m % 128 == 0) ? 2 : 1;   // same stage size as the gradients
+    p.epi.kind = EPI_OUT;
+    p.epi.out[0] = static_cast<char*>(a.out) + (long long)h0 * N * d * (long long)ios;
+    p.epi.out_ld = d;
+    p.epi.out_z = (long long)N * d;
+    p.epi.out_row0 = (long long)ap * b;
+    LB.add(p);
+  };
+  // this range's rows of output chunk ap are written (on stream s): copy them back
+  auto copy_out = [&](int ap, cudaStream_t s) -> int {
+    const size_t row = (size_t)b * d * ios, pitch = (size_t)N * d * ios;
+    const size_t off = ((size_t)h0 * N + (size_t)ap * b) * d * ios;
+    TTT_CK(cudaEventRecord(io->out_ev, s));
+    TTT_CK(cudaStreamWaitEvent(io->d2h, io->out_ev, 0));
+    TTT_CK(cudaMemcpy2DAsync(static_cast<char*>(a.host->out) + off, pitch,
+                             static_cast<const char*>(a.out) + off, pitch, row, nh,
+                             cudaMemcpyDeviceToHost, io->d2h));
+    return 0;
+  };
+
+  int waited = -1;   // host-buffer calls: last input chunk st waited for
   for (const auto& stp : L.steps) {
     const int ap = stp.first, up = stp.second;
-    if (io && std::max(ap, up) > waited) {
-      waited = std::max(ap, up);
+    const int need = split ? up : std::max(ap, up);
+    if (io && need > waited) {
+      waited = need;
       TTT_CK(cudaStreamWaitEvent(st, io->in_ev[std::min(waited, io->n_in - 1)], 0));
+    }
+    // ---------------- APPLY (own stream)
+    if (split && ap >= 0) {
+      TTT_CK(cudaStreamWaitEvent(sa, aev->ev_w, 0));
+      if (io) TTT_CK(cudaStreamWaitEvent(sa, io->in_ev[std::min(ap, io->n_in - 1)], 0));
+      add_apply_proj(ap);
+      if (!LB.ok()) return -4;
+      TTT_CK(LB.launch(sa, PT_APPLY_PROJ, 0, apply_ctas(nh)));
+      add_apply_out(ap);
+      if (!LB.ok()) return -4;
+      TTT_CK(LB.launch(sa, PT_APPLY_OUT, 0, apply_ctas(nh)));
+      if (io) {
+        const int rc = copy_out(ap, sa);
+        if (rc != 0) return rc;
+      }
+      TTT_CK(cudaEventRecord(aev->ev_a[cur], sa));
+      apply_reads[cur] = true;
     }
     // ---------------- PROJ
     if (up >= 0) {
       const int bn = LB.choose_bn(m, 3);
       Problem p = prob0(b, m, d, nh, 3, bn);
       p.a[0] = LB.op(L.Tk, 0, h0 * N + up * b, N, BM);
-      p.b[0] = LB.op(L.TW[0], 0, h0 * m, m, bn);
+      p.b[0] = LB.op(L.TW[cur][0], 0, h0 * m, m, bn);
       p.a[1] = p.a[0];
-      p.b[1] = LB.op(L.TW[1], 0, h0 * m, m, bn);
+      p.b[1] = LB.op(L.TW[cur][1], 0, h0 * m, m, bn);
       p.a[2] = LB.op(L.Tv, 0, h0 * N + up * b, N, BM);
-      p.b[2] = LB.op(L.TW[2], 1, h0 * d, d, bn);  // W2 [d, m]: K = d rows, N = m contiguous
+      p.b[2] = LB.op(L.TW[cur][2], 1, h0 * d, d, bn);  // W2 [d, m]: K = d rows, N = m contiguous
       p.a_shared = 1 << 1;
       p.epi.kind = EPI_PROJ_K;
       p.epi.out[0] = offs(w.dH1, h0 * bm_h);
@@ -227,22 +336,11 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
       p.epi.eta_row0 = (long long)up * b;
       LB.add(p);
     }
-    if (ap >= 0) {
-      const int bn = LB.choose_bn(m, 2);
-      Problem p = prob0(b, m, d, nh, 2, bn);
-      p.a[0] = LB.op(L.Tq, 0, h0 * N + ap * b, N, BM);
-      p.b[0] = LB.op(L.TW[0], 0, h0 * m, m, bn);
-      p.a[1] = p.a[0];
-      p.b[1] = LB.op(L.TW[1], 0, h0 * m, m, bn);
-      p.a_shared = 1 << 1;
-      p.epi.kind = EPI_PROJ_Q;
-      p.epi.out[0] = offs(w.Aq, h0 * bm_h);
-      p.epi.out_ld = m;
-      p.epi.out_z = bm_h;
-      LB.add(p);
+    if (!split && ap >= 0) add_apply_proj(ap);
+    if (up >= 0 || (!split && ap >= 0)) {
+      if (!LB.ok()) return -4;
+      TTT_CK(LB.launch(st, PT_PROJ, prio));
     }
-    if (!LB.ok()) return -4;
-    TTT_CK(LB.launch(st, PT_PROJ));
 
     // ---------------- GRAD (+ OUT)
     if (up >= 0) {
@@ -275,29 +373,14 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
         LB.add(p);
       }
     }
-    if (ap >= 0) {
-      const int bn = LB.choose_bn(d, 1);
-      Problem p = prob0(b, d, m, nh, 1, bn);
-      p.a[0] = LB.op(L.TAq, 0, h0 * b, b, BM);
-      p.b[0] = LB.op(L.TW[2], 0, h0 * d, d, bn);  // W2 [d, m]: N = d rows, K = m contiguous
-      p.kd = (tc && m % 128 == 0) ? 2 : 1;   // same stage size as the gradients
-      p.epi.kind = EPI_OUT;
-      p.epi.out[0] = static_cast<char*>(a.out) + (long long)h0 * N * d * (long long)ios;
-      p.epi.out_ld = d;
-      p.epi.out_z = (long long)N * d;
-      p.epi.out_row0 = (long long)ap * b;
-      LB.add(p);
+    if (!split && ap >= 0) add_apply_out(ap);
+    if (up >= 0 || (!split && ap >= 0)) {
+      if (!LB.ok()) return -4;
+      TTT_CK(LB.launch(st, PT_GRAD, prio));
     }
-    if (!LB.ok()) return -4;
-    TTT_CK(LB.launch(st, PT_GRAD));
-    if (io && ap >= 0) {   // this range's rows of output chunk ap are written: copy them back
-      const size_t row = (size_t)b * d * ios, pitch = (size_t)N * d * ios;
-      const size_t off = ((size_t)h0 * N + (size_t)ap * b) * d * ios;
-      TTT_CK(cudaEventRecord(io->out_ev, st));
-      TTT_CK(cudaStreamWaitEvent(io->d2h, io->out_ev, 0));
-      TTT_CK(cudaMemcpy2DAsync(static_cast<char*>(a.host->out) + off, pitch,
-                               static_cast<const char*>(a.out) + off, pitch, row, nh,
-                               cudaMemcpyDeviceToHost, io->d2h));
+    if (io && !split && ap >= 0) {
+      const int rc = copy_out(ap, st);
+      if (rc != 0) return rc;
     }
     if (after_first) {
       TTT_CK(cudaEventRecord(after_first, st));
@@ -305,6 +388,12 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
     }
 
     if (up < 0) continue;
+
+    const int nxt = split ? cur ^ 1 : cur;   // bf16 copy this update writes
+    if (split && apply_reads[nxt]) {         // the applies still reading it finish first
+      TTT_CK(cudaStreamWaitEvent(st, aev->ev_a[nxt], 0));
+      apply_reads[nxt] = false;
+    }
 
     // ---------------- MUON (Newton-Schulz on M, every matrix)
     bool fused_update = false;
@@ -320,7 +409,7 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
       na.nslot = w.nslot;
       for (int s = 0; s < 3; ++s) {
         na.W[s] = L.ms[s].master;
-        na.Wb[s] = L.ms[s].work;
+        na.Wb[s] = L.wb[nxt][s];
       }
       na.BH = BH;
       na.h0 = h0;
@@ -331,6 +420,7 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
       na.ns[0] = D.ns[0];
       na.ns[1] = D.ns[1];
       na.ns[2] = D.ns[2];
+      na.priority = prio;
       int rc = 1;
       if (use_ns_half(d)) rc = launch_ns_half(cache, na, L.status, L.wait_ns, st);
       if (rc == 1 && use_ns_panel(d)) rc = launch_ns_panel(cache, na, L.status, L.wait_ns, st);
@@ -447,12 +537,18 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
         const long long rc = (long long)rows_of[s] * cols_of[s];
         part[s] = L.ms[s];
         part[s].master = L.ms[s].master + h0 * rc;
-        part[s].work = L.ms[s].work ? static_cast<char*>(L.ms[s].work) + h0 * rc * 2 : nullptr;
+        part[s].work = L.wb[nxt][s] ? static_cast<char*>(L.wb[nxt][s]) + h0 * rc * 2 : nullptr;
         part[s].update = L.ms[s].update + h0 * rc;
       }
       ProfScope ps(PT_NORM, st, 0.0, 3.0 * nh * dm * (4 + 4 + 4 + (tc ? 2 : 0)));
       TTT_CK(launch_update_normalize(part, 3, nh, D.l2norm, st));
     }
+    cur = nxt;
+    if (split) TTT_CK(cudaEventRecord(aev->ev_w, st));
+  }
+  if (split) {   // join the apply stream
+    TTT_CK(cudaEventRecord(aev->ev_a[0], sa));
+    TTT_CK(cudaStreamWaitEvent(st, aev->ev_a[0], 0));
   }
   return 0;
 }
@@ -466,6 +562,17 @@ bool per_sequence_streams(const LayerDims& D) {
   if (D.muon_steps == 0) return true;
   return D.d == D.m && ((use_ns_half(D.d) && prepare_ns_half(D.d)) ||
                         (use_ns_panel(D.d) && prepare_ns_panel(D.d)) || prepare_ns_cluster(D.d));
+}
+
+// The apply side of every step runs on its own stream per group (bf16 path);
+// TTT_SPLIT_APPLY=0 keeps it in the update chain's launches instead.
+bool split_apply_on() {
+  static int v = -1;
+  if (v < 0) {
+    const char* s = std::getenv("TTT_SPLIT_APPLY");
+    v = (s && s[0] == '0') ? 0 : 1;
+  }
+  return v == 1;
 }
 
 // TTT_STAGGER=1 starts stream group g only after group g-1's first
@@ -482,9 +589,11 @@ bool stagger_on() {
 
 // Number of stream groups the (batch, head) sequences are split into: each
 // group's launches cover a contiguous range of sequences on its own stream.
-// The default is three groups (measured best on the 760M-scale layer, B*H = 8,
-// among 1 to 6: 4.41, 3.27, 3.19, 3.25, 3.26, 3.29 ms per step; smaller
-// Newton-Schulz launches pack better between the other groups' GEMMs);
+// The default is four groups with the apply side on its own streams, else
+// three (measured on the 760M-scale layer, B*H = 8: split, 3 / 4 groups: 2.97 /
+// 2.93 ms per step; unsplit, 1 to 6 groups: 4.41, 3.27, 3.19, 3.25, 3.26, 3.29
+// ms; smaller Newton-Schulz launches pack better between the other groups'
+// GEMMs);
 // TTT_SEQUENCE_GROUPS (1 .. B*H) overrides it, and 1 runs every launch batched
 // over all sequences on the caller's stream.
 int sequence_groups(const LayerDims& D) {
@@ -496,7 +605,8 @@ int sequence_groups(const LayerDims& D) {
     env = (s && s[0]) ? std::atoi(s) : -1;
   }
   if (env >= 1) return env < BH ? env : BH;
-  return BH < 3 ? BH : 3;
+  const int def = D.bf16 && split_apply_on() ? 4 : 3;
+  return BH < def ? BH : def;
 }
 
 // Host-buffer calls: chunks [c, c + n) of q, k, v and eta for every
@@ -533,16 +643,20 @@ int enqueue_all(LayerPlan& L, cudaStream_t st) {
   const int nc = D.N / D.chunk;
   const long long dm = (long long)D.d * D.m;
 
-  // streams: [0, ng) compute groups when ng > 1; host-buffer calls add one
-  // host-to-device stream and one device-to-host stream per group
+  // streams: [0, ng) compute groups when ng > 1, then one apply stream per
+  // group (bf16), then for host-buffer calls one host-to-device stream and one
+  // device-to-host stream per group.  Events per group: stagger, ev_w, ev_a[2].
+  const bool split = tc && split_apply_on();
   int ng = sequence_groups(D);
+  auto nstreams = [&](int g) { return (g > 1 ? g : 0) + (split ? g : 0) + (hio ? 1 + g : 0); };
   std::vector<cudaStream_t> pool;
-  std::vector<cudaEvent_t> stagger;
-  if (ng > 1 &&
-      !(stream_pool(ng + (hio ? 1 + ng : 0), &pool) && stagger_events(ng, &stagger)))
-    ng = 1;
-  if (ng == 1 && hio && !stream_pool(2, &pool)) return -6;
-  const int io0 = ng > 1 ? ng : 0;
+  std::vector<cudaEvent_t> sev;
+  if (ng > 1 && !(stream_pool(nstreams(ng), &pool) && stagger_events(4 * ng, &sev))) ng = 1;
+  if (ng == 1 && !(stream_pool(nstreams(1), &pool) && stagger_events(4, &sev))) return -6;
+  const int ap0 = ng > 1 ? ng : 0;
+  const int io0 = ap0 + (split ? ng : 0);
+  std::vector<ApplyEvents> aevs(ng);
+  for (int g = 0; g < ng; ++g) aevs[g] = ApplyEvents{sev[4 * g + 1], {sev[4 * g + 2], sev[4 * g + 3]}};
   std::vector<IoHooks> hooks(ng);
   std::vector<cudaEvent_t> evs;        // host-buffer calls: input chunks, then one per group
   std::vector<cudaEvent_t> chunk_ev;   // event of each input chunk
@@ -596,14 +710,16 @@ int enqueue_all(LayerPlan& L, cudaStream_t st) {
     // gradients enqueued.
     for (int g = 0; g < ng; ++g) {
       const int h0 = (int)((long long)BH * g / ng), h1 = (int)((long long)BH * (g + 1) / ng);
-      if (g > 0 && stagger_on()) TTT_CK(cudaStreamWaitEvent(kids[g], stagger[g - 1], 0));
-      const int rc = enqueue_range(L, cache, h0, h1 - h0, kids[g], stagger[g],
-                                   hio ? &hooks[g] : nullptr);
+      if (g > 0 && stagger_on()) TTT_CK(cudaStreamWaitEvent(kids[g], sev[4 * (g - 1)], 0));
+      const int rc = enqueue_range(L, cache, h0, h1 - h0, kids[g], sev[4 * g],
+                                   hio ? &hooks[g] : nullptr, split ? pool[ap0 + g] : nullptr,
+                                   split ? &aevs[g] : nullptr);
       if (rc != 0) return rc;
     }
     TTT_CK(join_streams(st, kids));
   } else {
-    const int rc = enqueue_range(L, cache, 0, BH, st, nullptr, hio ? &hooks[0] : nullptr);
+    const int rc = enqueue_range(L, cache, 0, BH, st, nullptr, hio ? &hooks[0] : nullptr,
+                                 split ? pool[ap0] : nullptr, split ? &aevs[0] : nullptr);
     if (rc != 0) return rc;
   }
   if (hio) {
@@ -657,9 +773,13 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
   L.Tq = TensorRef{a.q, wb16, (long long)BH * N, d};
   L.Tk = TensorRef{a.k, wb16, (long long)BH * N, d};
   L.Tv = TensorRef{a.v, wb16, (long long)BH * N, d};
-  for (int s = 0; s < 3; ++s)
-    L.TW[s] = TensorRef{tc ? w.Wb[s] : static_cast<const void*>(a.Wf[kPub[s]]), wb16,
-                        (long long)BH * rows_of[s], cols_of[s]};
+  for (int s = 0; s < 3; ++s) {
+    L.wb[0][s] = tc ? w.Wb[s] : nullptr;
+    L.wb[1][s] = tc ? w.Wb2[s] : nullptr;
+    for (int c = 0; c < 2; ++c)
+      L.TW[c][s] = TensorRef{tc ? L.wb[c][s] : static_cast<const void*>(a.Wf[kPub[s]]), wb16,
+                             (long long)BH * rows_of[s], cols_of[s]};
+  }
   L.TAq = TensorRef{w.Aq, wb16, (long long)BH * b, m};
   L.TdH1 = TensorRef{w.dH1, wb16, (long long)BH * b, m};
   L.TdH3 = TensorRef{w.dH3, wb16, (long long)BH * b, m};
@@ -710,6 +830,7 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
     key.push_back((uint64_t)h.momentum);
   }
   // one-time device setup outside any capture
+  high_priority();
   if (tc) {
     if (prepare_umma_gemm() != cudaSuccess) return -6;
     if (muon && d == m) {

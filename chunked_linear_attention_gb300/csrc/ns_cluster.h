@@ -20,6 +20,7 @@ struct NsArgs {
   int BH, d, steps, l2norm;
   int h0, nh;        // (batch, head) range handled by this launch: [h0, h0 + nh)
   float ns[3];
+  int priority = 0;  // launch priority (0: the stream's own)
 };
 
 // True if the cluster kernel handles d x d matrices; gives cluster size and N tile.

@@ -577,22 +577,26 @@ int launch_ns_half(MapCache& cache, const NsArgs& a, int* status, unsigned long 
   L.wait_limit_ns = wait_ns;
 
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
+  attr[2].id = cudaLaunchAttributePriority;
+  attr[2].val.priority = a.priority;
   cfg.gridDim = dim3(3 * a.nh * cs, 1, 1);
   cfg.blockDim = dim3(kHThreads, 1, 1);
   cfg.dynamicSmemBytes = kUmmaSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = a.priority != 0 ? 3 : 2;
   const double n3 = (double)d * d * d;
   const double flops = 3.0 * a.nh * a.steps * 6.0 * n3;
-  ProfScope ps(PT_MUON_HALF, stream, flops, 0.0);
+  const int sms = device_sm_count();
+  ProfScope ps(PT_MUON_HALF, stream, flops, 0.0,
+               sms > 0 ? (double)(3 * a.nh * cs) / sms : 1.0);
   if (cudaLaunchKernelEx(&cfg, ns_half_kernel, L) != cudaSuccess) return -6;
   return 0;
 }

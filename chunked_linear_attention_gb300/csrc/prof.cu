@@ -13,7 +13,7 @@ namespace {
 struct Rec {
   int tag;
   cudaEvent_t a, b;
-  double flops, bytes;
+  double flops, bytes, sm_share;
 };
 
 std::atomic<unsigned long long> g_launches{0};
@@ -24,12 +24,13 @@ std::vector<Rec> g_recs;
 const char* kTagName[PT_COUNT] = {
     "init", "gemm.proj", "gemm.grad", "gemm.ns_gram", "gemm.ns_poly", "gemm.ns_step",
     "norm", "lin.scale", "gemm.lin_partial", "lin.prefix", "gemm.lin_out", "gemm.selftest", "muon.cluster",
-    "muon.panel", "muon.half", "lin.fused"};
+    "muon.panel", "muon.half", "lin.fused", "gemm.apply_proj", "gemm.apply_out"};
 const char* kTagKernel[PT_COUNT] = {
     "init_layer_kernel", "umma_gemm_kernel", "umma_gemm_kernel", "umma_gemm_kernel",
     "umma_gemm_kernel", "umma_gemm_kernel", "update_normalize_kernel", "scale_rows_kernel",
     "umma_gemm_kernel", "linattn_prefix_kernel", "umma_gemm_kernel", "umma_gemm_kernel",
-    "ns_cluster_kernel", "ns_panel_kernel", "ns_half_kernel", "linattn_fused_kernel"};
+    "ns_cluster_kernel", "ns_panel_kernel", "ns_half_kernel", "linattn_fused_kernel",
+    "umma_gemm_kernel", "umma_gemm_kernel"};
 
 }  // namespace
 
@@ -40,13 +41,15 @@ bool prof_recording() {
 
 void prof_count_launches(size_t n) { g_launches.fetch_add(n); }
 
-ProfScope::ProfScope(int tag, cudaStream_t s, double flops, double bytes) : idx_(-1), s_(s) {
+ProfScope::ProfScope(int tag, cudaStream_t s, double flops, double bytes, double sm_share)
+    : idx_(-1), s_(s) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (!g_on) return;
   Rec r;
   r.tag = tag;
   r.flops = flops;
   r.bytes = bytes;
+  r.sm_share = sm_share < 1.0 ? sm_share : 1.0;
   if (cudaEventCreate(&r.a) != cudaSuccess) return;
   if (cudaEventCreate(&r.b) != cudaSuccess) {
     cudaEventDestroy(r.a);
@@ -94,6 +97,7 @@ int ttt_profile_stop(ttt_profile_entry* entries, int max_entries) {
     acc[r.tag].ms += ms;
     acc[r.tag].flops += r.flops;
     acc[r.tag].bytes += r.bytes;
+    acc[r.tag].sm_ms += ms * r.sm_share;
     cudaEventDestroy(r.a);
     cudaEventDestroy(r.b);
   }

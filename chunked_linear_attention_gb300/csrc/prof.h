@@ -23,6 +23,8 @@ enum ProfTag : int {
   PT_MUON_PANEL,
   PT_MUON_HALF,
   PT_LIN_FUSED,
+  PT_APPLY_PROJ,
+  PT_APPLY_OUT,
   PT_COUNT
 };
 
@@ -36,7 +38,8 @@ void prof_count_launches(size_t n);
 // records the one after and counts the launch.
 class ProfScope {
  public:
-  ProfScope(int tag, cudaStream_t s, double flops, double bytes);
+  // `sm_share`: fraction of the device's SMs the launch's grid holds (<= 1).
+  ProfScope(int tag, cudaStream_t s, double flops, double bytes, double sm_share = 1.0);
   ~ProfScope();
 
  private:

@@ -24,6 +24,8 @@ typedef struct {
   double ms;       /* summed device time of those launches */
   double flops;    /* summed algorithmic FLOPs (matrix products) */
   double bytes;    /* summed algorithmic DRAM bytes (bandwidth kernels) */
+  double sm_ms;    /* summed device time x the fraction of the SMs each launch's
+                      grid holds (at most 1): the GPU time the launches occupy */
 } ttt_profile_entry;
 
 /* Total kernel launches the library has made in this process. */
