@@ -203,6 +203,16 @@ int apply_ctas(int nh) {
   return v * nh;
 }
 
+// TTT_CHAIN_PRIORITY=0 launches the update chain at the streams' own priority.
+bool chain_priority_on() {
+  static int v = -1;
+  if (v < 0) {
+    const char* s = std::getenv("TTT_CHAIN_PRIORITY");
+    v = (s && s[0] == '0') ? 0 : 1;
+  }
+  return v == 1;
+}
+
 // The apply side of a step (query projections and the output GEMM of its
 // apply chunk) depends only on that step's weights, and nothing in the scan
 // depends on it.  With an apply stream `sa` it runs there, overlapping the
@@ -239,7 +249,7 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
   const long long bm_h = (long long)b * m;   // activation elements per (batch, head)
   const bool split = sa != nullptr && aev != nullptr;
   // the update chain's launches go first; the apply side fills the SMs they leave
-  const int prio = split ? high_priority() : 0;
+  const int prio = split && chain_priority_on() ? high_priority() : 0;
   int cur = 0;                           // bf16 copy holding the current weights
   bool apply_reads[2] = {false, false};  // an apply that st has not waited for reads copy c
 
@@ -596,7 +606,7 @@ bool stagger_on() {
 // GEMMs);
 // TTT_SEQUENCE_GROUPS (1 .. B*H) overrides it, and 1 runs every launch batched
 // over all sequences on the caller's stream.
-int sequence_groups(const LayerDims& D) {
+int sequence_groups(const LayerDims& D, bool split) {
   const int BH = D.B * D.H;
   if (!per_sequence_streams(D)) return 1;
   static int env = -2;
@@ -605,7 +615,7 @@ int sequence_groups(const LayerDims& D) {
     env = (s && s[0]) ? std::atoi(s) : -1;
   }
   if (env >= 1) return env < BH ? env : BH;
-  const int def = D.bf16 && split_apply_on() ? 4 : 3;
+  const int def = split ? 4 : 3;
   return BH < def ? BH : def;
 }
 
@@ -644,10 +654,13 @@ int enqueue_all(LayerPlan& L, cudaStream_t st) {
   const long long dm = (long long)D.d * D.m;
 
   // streams: [0, ng) compute groups when ng > 1, then one apply stream per
-  // group (bf16), then for host-buffer calls one host-to-device stream and one
-  // device-to-host stream per group.  Events per group: stagger, ev_w, ev_a[2].
-  const bool split = tc && split_apply_on();
-  int ng = sequence_groups(D);
+  // group (bf16 device-buffer calls), then for host-buffer calls one
+  // host-to-device stream and one device-to-host stream per group.  Events per
+  // group: stagger, ev_w, ev_a[2].  Host-buffer calls keep the apply side in
+  // the chain's launches: with the extra streams their input copies stalled
+  // behind queued kernels (8-9 ms per call instead of 4.7 ms).
+  const bool split = tc && !hio && split_apply_on();
+  int ng = sequence_groups(D, split);
   auto nstreams = [&](int g) { return (g > 1 ? g : 0) + (split ? g : 0) + (hio ? 1 + g : 0); };
   std::vector<cudaStream_t> pool;
   std::vector<cudaEvent_t> sev;
