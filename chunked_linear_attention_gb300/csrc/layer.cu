@@ -190,17 +190,21 @@ struct IoHooks {
 // CTAs of each apply-side launch for `nh` sequences (TTT_APPLY_CTAS sets the
 // CTAs per sequence): the persistent GEMM keeps its CTAs for the whole launch,
 // so the apply side is held to a share of the SMs and the update chain finds
-// the rest free.  Measured on the 760M-scale layer (four groups of two
-// sequences): 2, 3, 4, 6 CTAs per sequence -> 3.04, 2.90, 2.93, 2.95 ms per
-// step; uncapped (152 CTAs) 3.2 ms, and 3.11 ms without the split.
-int apply_ctas(int nh) {
+// the rest free, while the applies of a step must still finish within about
+// one step of the chain.  Measured on the 760M-scale layer with 5 Muon steps
+// (four groups of two sequences): 2, 3, 4, 6 CTAs per sequence -> 3.04, 2.90,
+// 2.93, 2.95 ms per step; uncapped (152 CTAs) 3.2 ms, and 3.11 ms without the
+// split.  The chain shortens with fewer Muon steps, so the default share
+// grows as 15 / steps CTAs per sequence (only 5 steps measured).
+int apply_ctas(int nh, int muon_steps) {
   static int v = -1;
   if (v < 0) {
     const char* s = std::getenv("TTT_APPLY_CTAS");
-    v = (s && s[0]) ? std::atoi(s) : 3;
+    v = (s && s[0]) ? std::atoi(s) : 0;
     if (v < 0) v = 0;
   }
-  return v * nh;
+  const int per = v > 0 ? v : (15 + muon_steps - 1) / muon_steps;
+  return per * nh;
 }
 
 // TTT_CHAIN_PRIORITY=0 launches the update chain at the streams' own priority.
@@ -313,10 +317,10 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
       if (io) TTT_CK(cudaStreamWaitEvent(sa, io->in_ev[std::min(ap, io->n_in - 1)], 0));
       add_apply_proj(ap);
       if (!LB.ok()) return -4;
-      TTT_CK(LB.launch(sa, PT_APPLY_PROJ, 0, apply_ctas(nh)));
+      TTT_CK(LB.launch(sa, PT_APPLY_PROJ, 0, apply_ctas(nh, D.muon_steps)));
       add_apply_out(ap);
       if (!LB.ok()) return -4;
-      TTT_CK(LB.launch(sa, PT_APPLY_OUT, 0, apply_ctas(nh)));
+      TTT_CK(LB.launch(sa, PT_APPLY_OUT, 0, apply_ctas(nh, D.muon_steps)));
       if (io) {
         const int rc = copy_out(ap, sa);
         if (rc != 0) return rc;
@@ -600,10 +604,11 @@ bool stagger_on() {
 // Number of stream groups the (batch, head) sequences are split into: each
 // group's launches cover a contiguous range of sequences on its own stream.
 // The default is four groups with the apply side on its own streams, else
-// three (measured on the 760M-scale layer, B*H = 8: split, 3 / 4 groups: 2.97 /
-// 2.93 ms per step; unsplit, 1 to 6 groups: 4.41, 3.27, 3.19, 3.25, 3.26, 3.29
-// ms; smaller Newton-Schulz launches pack better between the other groups'
-// GEMMs);
+// three with Muon and one without (measured on the 760M-scale layer, B*H = 8:
+// split, 3 / 4 groups: 2.97 / 2.93 ms per step; unsplit, 1 to 6 groups: 4.41,
+// 3.27, 3.19, 3.25, 3.26, 3.29 ms; smaller Newton-Schulz launches pack better
+// between the other groups' GEMMs; without Muon 1 / 3 / 4 groups: 1.56 / 1.67
+// / 1.76 ms);
 // TTT_SEQUENCE_GROUPS (1 .. B*H) overrides it, and 1 runs every launch batched
 // over all sequences on the caller's stream.
 int sequence_groups(const LayerDims& D, bool split) {
@@ -615,7 +620,7 @@ int sequence_groups(const LayerDims& D, bool split) {
     env = (s && s[0]) ? std::atoi(s) : -1;
   }
   if (env >= 1) return env < BH ? env : BH;
-  const int def = split ? 4 : 3;
+  const int def = split ? 4 : (D.muon_steps > 0 ? 3 : 1);
   return BH < def ? BH : def;
 }
 
@@ -658,8 +663,10 @@ int enqueue_all(LayerPlan& L, cudaStream_t st) {
   // host-to-device stream and one device-to-host stream per group.  Events per
   // group: stagger, ev_w, ev_a[2].  Host-buffer calls keep the apply side in
   // the chain's launches: with the extra streams their input copies stalled
-  // behind queued kernels (8-9 ms per call instead of 4.7 ms).
-  const bool split = tc && !hio && split_apply_on();
+  // behind queued kernels (8-9 ms per call instead of 4.7 ms).  Without Muon
+  // the update chain is short and the capped apply side would set the pace
+  // (1.93 ms per step against 1.56 ms unsplit), so only Muon runs split.
+  const bool split = tc && !hio && D.muon_steps > 0 && split_apply_on();
   int ng = sequence_groups(D, split);
   auto nstreams = [&](int g) { return (g > 1 ? g : 0) + (split ? g : 0) + (hio ? 1 + g : 0); };
   std::vector<cudaStream_t> pool;

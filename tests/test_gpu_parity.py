@@ -296,11 +296,15 @@ def test_layer_bitwise_repeatable():
         assert np.array_equal(a_, b_)
 
 
-# Two workloads that exercise both update paths: the fused Newton-Schulz launch
-# (Muon, apply and update of the same chunk every step) and the normalisation
-# launch (no Muon, strided update flags: steps that only apply or only update).
+# Workloads that exercise every update path: the fused Newton-Schulz launch
+# (Muon, apply and update of the same chunk every step), the per-product
+# Newton-Schulz launches and the normalisation launch (non-square weights,
+# strided update flags: steps that only apply or only update), and the
+# normalisation alone (no Muon).
 SCHED_WORKLOADS = [
     dict(B=2, H=2, N=2048, d_h=256, m_h=256, chunk=256, muon_steps=5, momentum_beta=0.9),
+    dict(B=1, H=2, N=1024, d_h=128, m_h=256, chunk=128, muon_steps=2, momentum_beta=0.5,
+         mode=W.STRIDED, update_chunks=(1, 0, 0, 1, 0, 1, 1, 0)),
     dict(B=1, H=3, N=1024, d_h=128, m_h=256, chunk=128, muon_steps=0, momentum_beta=0.5,
          mode=W.STRIDED, update_chunks=(1, 0, 0, 1, 0, 1, 1, 0)),
 ]
