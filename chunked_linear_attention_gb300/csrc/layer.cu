@@ -26,6 +26,7 @@
 // Matrix slots: 0 = W1 [m, d], 1 = W3 [m, d], 2 = W2 [d, m]; every
 // per-matrix buffer is [slot][B*H][rows*cols].
 #include <algorithm>
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <vector>
@@ -194,17 +195,20 @@ struct IoHooks {
 // one step of the chain.  Measured on the 760M-scale layer with 5 Muon steps
 // (four groups of two sequences): 2, 3, 4, 6 CTAs per sequence -> 3.04, 2.90,
 // 2.93, 2.95 ms per step; uncapped (152 CTAs) 3.2 ms, and 3.11 ms without the
-// split.  The chain shortens with fewer Muon steps, so the default share
-// grows as 15 / steps CTAs per sequence (only 5 steps measured).
-int apply_ctas(int nh, int muon_steps) {
+// split.  The default share grows with the apply work per sequence and chunk
+// (b d m, relative to that layer's 2048 x 384 x 384), so that a step's applies
+// keep taking about as long, and as 15 / steps with fewer Muon steps, as the
+// chain then gets shorter (only that layer and 5 steps measured).
+int apply_ctas(int nh, int muon_steps, const LayerDims& D) {
   static int v = -1;
   if (v < 0) {
     const char* s = std::getenv("TTT_APPLY_CTAS");
     v = (s && s[0]) ? std::atoi(s) : 0;
     if (v < 0) v = 0;
   }
-  const int per = v > 0 ? v : (15 + muon_steps - 1) / muon_steps;
-  return per * nh;
+  const double work = (double)D.chunk * D.d * D.m / (2048.0 * 384.0 * 384.0);
+  const double per = v > 0 ? (double)v : 15.0 / muon_steps * (work > 1.0 ? work : 1.0);
+  return (int)std::ceil(per * nh);
 }
 
 // The chain's GEMM launches rank one priority level below its Newton-Schulz
@@ -331,10 +335,10 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
       if (io) TTT_CK(cudaStreamWaitEvent(sa, io->in_ev[std::min(ap, io->n_in - 1)], 0));
       add_apply_proj(ap);
       if (!LB.ok()) return -4;
-      TTT_CK(LB.launch(sa, PT_APPLY_PROJ, 0, apply_ctas(nh, D.muon_steps)));
+      TTT_CK(LB.launch(sa, PT_APPLY_PROJ, 0, apply_ctas(nh, D.muon_steps, D)));
       add_apply_out(ap);
       if (!LB.ok()) return -4;
-      TTT_CK(LB.launch(sa, PT_APPLY_OUT, 0, apply_ctas(nh, D.muon_steps)));
+      TTT_CK(LB.launch(sa, PT_APPLY_OUT, 0, apply_ctas(nh, D.muon_steps, D)));
       if (io) {
         const int rc = copy_out(ap, sa);
         if (rc != 0) return rc;
