@@ -69,3 +69,19 @@ def test_reference_arm_other_ranks_exit_without_work(monkeypatch, capsys):
 
     assert bench.run_reference(A()) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_roofline_entry_per_launch_and_held_sm_rates():
+    """The roofline object: FLOPs per launch over the average launch duration
+    against the peak, plus the rate on the SMs the launches hold (device time x
+    SM share)."""
+    import bench
+    agg = {"launches": 4, "ms": 0.4, "flops": 4.0e12 * 0.4e-3, "sm_ms": 0.1}
+    r = bench.roofline_entry("no_such_kernel", agg, 2000.0, "test")
+    assert r["kernel"] == "no_such_kernel" and r["bound"] == "tensor"
+    assert abs(r["achieved"] - 4.0) < 1e-9               # 0.4 GFLOP per 0.1 ms launch
+    assert abs(r["frac"] - 0.002) < 1e-12
+    assert abs(r["avg_launch_us"] - 100.0) < 1e-9
+    assert abs(r["avg_sm_share"] - 0.25) < 1e-12
+    assert abs(r["achieved_on_held_sms"] - 16.0) < 1e-9  # same FLOPs over a quarter of the time
+    assert r["traffic"] is None                           # no committed summary for it
