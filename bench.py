@@ -10,17 +10,23 @@ bf16 q/k/v (L2-normed keys), fp32 fast weights; seeded synthetic inputs from
 sequence (every chunk: projections + gating, weight gradients, momentum,
 Muon, normalisation, apply).
 
-Under torchrun with N ranks every rank runs its own copy of the workload on
-its own GPU (weak scaling, no collective on the data path); rank 0 prints one
-JSON line.  ``--impl reference`` times the fp64 CPU oracle instead, on a
-bounded sample of the same workload.
+The same line carries the view-synthesis strided workload (B1 H2 d384
+m768, 8 chunks of 8192, update on chunks 0-3) and the million-token context
+(B1 H4 d=m=512, N = 1,048,576, chunk 8192, Muon 5) under "workloads";
+``--workload`` makes either of them the headline instead.
+
+The library is single-GPU: its Newton-Schulz kernels use TMA multicast
+within a thread-block cluster, which is kept to one-GPU jobs.  A launch on
+more than one GPU (``--gpus N`` with N > 1, or torchrun with WORLD_SIZE > 1)
+prints one line saying so and exits 0 without touching a GPU.
+``--impl reference`` times the fp64 CPU oracle instead, on a bounded sample of
+the same workload (rank 0 only under torchrun).
 """
 from __future__ import annotations
 
 import argparse
 import dataclasses
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -38,41 +44,26 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 # ---------------------------------------------------------------------------
-# distributed plumbing (weak scaling: each rank runs its own workload copy)
+# process layout: one process, one GPU
 
 def dist_env():
+    """(rank, world size, local rank) from the launcher's environment."""
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
-def init_dist(backend: str):
-    import torch.distributed as dist
-    rank, world, _ = dist_env()
-    if world > 1 and not dist.is_initialized():
-        dist.init_process_group(backend=backend)
-    return rank, world
-
-
-def barrier():
-    import torch.distributed as dist
-    if dist.is_available() and dist.is_initialized():
-        dist.barrier()
-
-
-def reduce_max(x: float, device=None) -> float:
-    """Maximum of x over ranks (x itself on one rank)."""
-    import torch
-    import torch.distributed as dist
-    if not (dist.is_available() and dist.is_initialized()):
-        return float(x)
-    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
-def aggregate_throughput(units_per_rank: float, world: int, max_seconds: float) -> float:
-    """Whole-job throughput: the units every rank processed over the slowest rank's time."""
-    return units_per_rank * world / max_seconds
+def single_gpu_refusal(args):
+    """The line printed instead of a measurement when the job spans more than
+    one GPU (None when it does not)."""
+    _, world, _ = dist_env()
+    n = max(world, args.gpus)
+    if n <= 1:
+        return None
+    return {"metric": METRIC, "value": None, "unit": UNIT, "n_gpus": n, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True,
+            "unavailable": "single-GPU build: the Newton-Schulz kernels use TMA cluster multicast, "
+                           "which is kept to one-GPU jobs; the layer shards only as independent "
+                           "replicas and no replica mode is provided"}
 
 
 # ---------------------------------------------------------------------------
@@ -91,7 +82,7 @@ class ClockSampler:
 
     def start(self):
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-               "-lms", "100"]
+               "-lms", "25"]
         if self.gpu_index is not None:
             cmd += ["-i", str(self.gpu_index)]
         try:
@@ -181,34 +172,56 @@ def cpu_cores() -> int:
 # ---------------------------------------------------------------------------
 # the oracle on a bounded sample (CPU baseline / reference arm)
 
-def oracle_sample(wl, inputs, budget_s: float = 12.0, chunks_per_run: int = 2):
-    """Runs the fp64 oracle, as it stands, on the first ``chunks_per_run``
-    chunks of one (batch, head) sequence after another until about
-    ``budget_s`` seconds have passed.  Every chunk does the same work, so the
-    rate extrapolates to the whole workload.  Returns (layer tokens/s, sample
-    description, seconds)."""
+def oracle_sample(wl, budget_s: float = 12.0, max_chunks: int = 2):
+    """Runs the fp64 oracle, as it stands, on one (batch, head) sequence after
+    another until about ``budget_s`` seconds have passed, each run covering
+    the first ``max_chunks`` chunks of the workload (every chunk of a
+    strided workload, whose chunks differ in work).  The inputs are drawn
+    with the workload's recipe at the sampled length.  Every sampled run
+    does the work of the same chunks, so the rate extrapolates to the whole
+    workload.  Returns (layer tokens/s, sample description, seconds)."""
+    import workloads
     from oracle import ttt_oracle as O
-    q, k, v, eta, W1, W2, W3 = inputs
-    n = min(chunks_per_run, wl.N // wl.chunk)
-    sl = slice(0, n * wl.chunk)
+    nc = wl.N // wl.chunk
+    n = nc if wl.update_chunks is not None else min(max_chunks, nc)
+    q, k, v, eta, W1, W2, W3 = workloads.layer_inputs(wl, B=1, H=1, N=n * wl.chunk)
+    x = [t.double().numpy() for t in (q, k, v)]
+    e = eta.double().numpy()
+    w = [t.double().numpy() for t in (W1, W2, W3)]
+    flags = None if wl.update_chunks is None else list(wl.update_chunks)[:n]
     runs, elapsed = 0, 0.0
-    pairs = [(b, h) for b in range(wl.B) for h in range(wl.H)]
     while elapsed < budget_s:
-        b, h = pairs[runs % len(pairs)]
-        x = [t[b:b + 1, h:h + 1, sl].double().numpy() for t in (q, k, v)]
-        e = eta[b:b + 1, h:h + 1, sl].double().numpy()
-        w = [t[h:h + 1].double().numpy() for t in (W1, W2, W3)]
         ts = time.perf_counter()
-        O.ttt_layer_forward(*x, e, *w, wl.chunk, wl.mode, l2norm=wl.l2norm,
+        O.ttt_layer_forward(*x, e, *w, wl.chunk, wl.mode, update_chunks=flags, l2norm=wl.l2norm,
                             muon_steps=wl.muon_steps, momentum_beta=wl.momentum_beta)
         elapsed += time.perf_counter() - ts
         runs += 1
     head_tokens = runs * n * wl.chunk
     rate = head_tokens / elapsed / wl.H   # every layer token costs H head-tokens
-    desc = (f"fp64 oracle on the first {n} chunks of {runs} (batch, head) sequences of the "
-            f"workload ({head_tokens} head-tokens in {elapsed:.1f} s); layer tokens/s = "
-            f"head-tokens/s / H")
+    desc = (f"fp64 oracle on the first {n} of {nc} chunks of one (batch, head) sequence, "
+            f"{runs} runs ({head_tokens} head-tokens in {elapsed:.1f} s); "
+            f"layer tokens/s = head-tokens/s / H")
     return rate, desc, elapsed
+
+
+# workloads bench.py can time (--workload); the default is the first
+WORKLOADS = ("lm760m", "nvs-strided", "long-1m")
+
+
+def workload_by_key(key):
+    import workloads
+    return {"lm760m": workloads.LM_760M, "nvs-strided": workloads.NVS_STRIDED,
+            "long-1m": workloads.LONG_1M}[key]
+
+
+def workload_config(wl):
+    mask = {0: "apply-then-update", 1: "block-causal", 2: "bidirectional", 3: "strided"}[wl.mode]
+    cfg = {"workload": wl.name, "B": wl.B, "H": wl.H, "N": wl.N, "d_h": wl.d_h, "m_h": wl.m_h,
+           "chunk": wl.chunk, "mask": mask, "muon_steps": wl.muon_steps,
+           "momentum_beta": wl.momentum_beta, "l2norm": wl.l2norm}
+    if wl.update_chunks is not None:
+        cfg["update_chunks"] = list(wl.update_chunks)
+    return cfg
 
 
 # ---------------------------------------------------------------------------
@@ -218,25 +231,23 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    import workloads
-    wl = workloads.LM_760M
-    inputs = workloads.layer_inputs(wl)
+    wl = workload_by_key(args.workload)
     per_step = []
     for _ in range(args.warmup):
-        oracle_sample(wl, inputs, budget_s=1.0)
+        oracle_sample(wl, budget_s=1.0)
+    desc = ""
     for _ in range(args.steps):
-        rate, desc, el = oracle_sample(wl, inputs, budget_s=args.ref_budget)
+        rate, desc, el = oracle_sample(wl, budget_s=args.ref_budget)
         per_step.append(rate)
     value = statistics.median(per_step)
+    cfg = workload_config(wl)
+    cfg["parallelism"] = "single process (host cores)"
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": max(world, args.gpus), "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": wl.B * wl.N / value * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "N": wl.N, "d_h": wl.d_h,
-                   "m_h": wl.m_h, "chunk": wl.chunk, "mask": "apply-then-update",
-                   "muon_steps": wl.muon_steps, "momentum_beta": wl.momentum_beta,
-                   "l2norm": wl.l2norm, "parallelism": "replicas"},
+        "config": cfg,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -250,9 +261,6 @@ KERNEL_PROFILE = {
     "ns_half_kernel": ("profiles/ns_half_kernel_lm760m.md",
                        ("chunked_linear_attention_gb300/csrc/ns_half.cu",
                         "chunked_linear_attention_gb300/csrc/common.cuh")),
-    "ns_panel_kernel": ("profiles/ns_panel_kernel_lm760m.md",
-                        ("chunked_linear_attention_gb300/csrc/ns_panel.cu",
-                         "chunked_linear_attention_gb300/csrc/common.cuh")),
     "umma_gemm_kernel": ("profiles/umma_gemm_kernel_lm760m.md",
                          ("chunked_linear_attention_gb300/csrc/gemm_umma.cu",
                           "chunked_linear_attention_gb300/csrc/umma_core.cuh",
@@ -317,10 +325,10 @@ def roofline_entry(name, agg, peak, peak_src):
 
 
 def time_steps(torch, fn, steps, warmup, stream):
+    """CUDA-event time (ms) of `steps` calls of fn after `warmup` untimed ones,
+    with the device synchronised on both sides."""
     for _ in range(warmup):
         fn()
-    torch.cuda.synchronize()
-    barrier()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -329,85 +337,178 @@ def time_steps(torch, fn, steps, warmup, stream):
         fn()
     e1.record(stream)
     torch.cuda.synchronize()
-    barrier()
     return e0.elapsed_time(e1)
+
+
+# inputs above this many q elements are drawn on the device
+HOST_DRAW_LIMIT = 1 << 28
+
+
+def device_inputs(torch, wl, dev):
+    """(device inputs, page-locked host copies or None) for a layer workload."""
+    import workloads
+    if wl.B * wl.H * wl.N * wl.d_h > HOST_DRAW_LIMIT:
+        return list(workloads.layer_inputs_on_device(wl, dev)), None
+    pinned = [t.pin_memory() for t in workloads.layer_inputs(wl)]
+    return [t.to(dev) for t in pinned], pinned
+
+
+class LayerCall:
+    """One ttt_layer_forward call over a workload with preallocated outputs
+    and workspace (device-resident inputs)."""
+
+    def __init__(self, torch, cla, wl, dev, inputs):
+        self.cla, self.wl = cla, wl
+        self.q, self.k, self.v, self.eta, self.W1, self.W2, self.W3 = inputs
+        B, H, N, d, m, b = wl.B, wl.H, wl.N, wl.d_h, wl.m_h, wl.chunk
+        self.rule = cla.update_rule(l2norm=wl.l2norm, muon_steps=wl.muon_steps,
+                                    momentum_beta=wl.momentum_beta)
+        self.out = torch.empty_like(self.q)
+        self.Wf = (torch.empty((B, H, m, d), device=dev), torch.empty((B, H, d, m), device=dev),
+                   torch.empty((B, H, m, d), device=dev))
+        self.ws = torch.empty(cla.layer_workspace_size(B, H, N, d, m, b, cla.TTT_BF16, wl.mode,
+                                                       self.rule), device=dev, dtype=torch.uint8)
+
+    def __call__(self):
+        self.cla.ttt_layer_forward(self.q, self.k, self.v, self.eta, self.W1, self.W2, self.W3,
+                                   self.wl.chunk, self.wl.mode, self.rule,
+                                   update_chunks=self.wl.update_chunks, out=self.out,
+                                   W_final=self.Wf, workspace=self.ws)
+
+
+def check_status(cla):
+    st = cla.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {cla.status_string(st)}")
+
+
+def time_extra_workload(torch, cla, wl, dev, stream, peaks, steps, warmup):
+    """ms per call, tokens/s and share of the bf16 peak of a further workload."""
+    inputs, _ = device_inputs(torch, wl, dev)
+    call = LayerCall(torch, cla, wl, dev, inputs)
+    call()
+    torch.cuda.synchronize()
+    check_status(cla)
+    ms = time_steps(torch, call, steps, warmup, stream) / steps
+    check_status(cla)
+    fl = layer_flops(wl)
+    tfl = fl / (ms / 1e3) / 1e12
+    res = {"config": workload_config(wl), "ms_per_call": ms, "steps": steps, "warmup": warmup,
+           "tokens_per_s": wl.B * wl.N / (ms / 1e3), "flops_per_call": fl, "tflops": tfl,
+           "frac_of_burst": tfl / float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
+           "inputs": "drawn on the device" if wl.B * wl.H * wl.N * wl.d_h > HOST_DRAW_LIMIT
+           else "drawn on the host, copied once"}
+    del call, inputs
+    torch.cuda.empty_cache()
+    return res
+
+
+def time_linattn(torch, cla, dev, stream, peaks):
+    """The chunked linear-attention workload (HBM-bound): L2 flushed before
+    every call, CUDA-event time of the call alone."""
+    import workloads
+    lw = workloads.LINATTN_C2
+    lq, lk, lv, leta, _ = [t.to(dev) if t is not None else None
+                           for t in workloads.linattn_inputs(lw)]
+    lo = torch.empty_like(lq)
+    lS = torch.empty((lw.B, lw.H, lw.d_v, lw.d_k), device=dev)
+    lws = torch.empty(cla.linattn_workspace_size(lw.B, lw.H, lw.N, lw.d_k, lw.d_v, lw.chunk,
+                                                 cla.TTT_BF16, lw.mode),
+                      device=dev, dtype=torch.uint8)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    tot, reps = 0.0, 20
+    for i in range(reps + 3):
+        flush.zero_()    # evict the inputs from L2 between repetitions
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        cla.linattn_chunked_forward(lq, lk, lv, leta, lw.chunk, lw.mode, out=lo, S_final=lS,
+                                    workspace=lws)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            tot += e0.elapsed_time(e1)
+    check_status(cla)
+    lms = tot / reps
+    io_bytes = (3 * lq.numel() * 2 + leta.numel() * 4 + lo.numel() * 2)
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    return {"workload": lw.name, "us_per_call": lms * 1e3,
+            "tokens_per_s": lw.B * lw.N / (lms / 1e3),
+            "gbs": io_bytes / (lms / 1e3) / 1e9, "hbm_frac": io_bytes / (lms / 1e3) / 1e9 / hbm,
+            "io_bytes": io_bytes, "l2": "flushed (256 MB write) before each call"}
 
 
 def run_ours(args):
     import torch
     import chunked_linear_attention_gb300 as cla
-    import workloads
     from chunked_linear_attention_gb300 import _build
 
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    init_dist("nccl")
+    refusal = single_gpu_refusal(args)
+    if refusal is not None:
+        if dist_env()[0] == 0:
+            print(json.dumps(refusal), flush=True)
+        return 0
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
     _build.build()
     cla.library()
 
-    wl = workloads.LM_760M
+    wl = workload_by_key(args.workload)
     if args.seq_len:
-        wl = dataclasses.replace(wl, N=args.seq_len)
+        wl = dataclasses.replace(wl, N=args.seq_len,
+                                 update_chunks=None if wl.update_chunks is None
+                                 else wl.update_chunks[:args.seq_len // wl.chunk])
     B, H, N, d, m, b = wl.B, wl.H, wl.N, wl.d_h, wl.m_h, wl.chunk
-    host = workloads.layer_inputs(wl, seed=wl.seed + rank)
-    pinned = [t.pin_memory() for t in host]
-    q, k, v, eta, W1, W2, W3 = [t.to(dev) for t in pinned]
-    rule = cla.update_rule(l2norm=wl.l2norm, muon_steps=wl.muon_steps,
-                           momentum_beta=wl.momentum_beta)
-    out = torch.empty_like(q)
-    Wf = (torch.empty((B, H, m, d), device=dev), torch.empty((B, H, d, m), device=dev),
-          torch.empty((B, H, m, d), device=dev))
-    ws = torch.empty(cla.layer_workspace_size(B, H, N, d, m, b, cla.TTT_BF16, wl.mode, rule),
-                     device=dev, dtype=torch.uint8)
+    inputs, pinned = device_inputs(torch, wl, dev)
+    step = LayerCall(torch, cla, wl, dev, inputs)
     stream = torch.cuda.current_stream(dev)
-
-    def step():
-        cla.ttt_layer_forward(q, k, v, eta, W1, W2, W3, b, wl.mode, rule, out=out, W_final=Wf,
-                              workspace=ws)
+    peaks, peak_src = load_peaks()
 
     # device-resident timing, clocks sampled during the timed region
-    clocks = ClockSampler(gpu_index=None if world > 1 else local)
+    clocks = ClockSampler(gpu_index=dev.index)
     step()
     torch.cuda.synchronize()
-    st = cla.device_status()
-    if st != 0:
-        raise RuntimeError(f"device status {st}: {cla.status_string(st)}")
+    check_status(cla)
     launches0 = cla.launch_count()
     clocks.start()
     ms = time_steps(torch, step, args.steps, args.warmup, stream)
     clk = clocks.stop()
+    check_status(cla)
     launches = (cla.launch_count() - launches0) // (args.steps + args.warmup) * args.steps
-    max_ms = reduce_max(ms, dev)
-    ms_step = max_ms / args.steps
+    ms_step = ms / args.steps
     tokens = B * N
-    value = aggregate_throughput(tokens * args.steps, world, max_ms / 1e3)
+    value = tokens * args.steps / (ms / 1e3)
 
     # end to end through the public host-buffer call: page-locked inputs in,
     # outputs and final weights back in page-locked host memory; the library
     # overlaps each chunk's transfers with the kernels
-    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    h_W = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in Wf]
+    if pinned is None:
+        pinned = [t.cpu().pin_memory() for t in inputs]
+    h_out = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
+    h_W = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in step.Wf]
     hq, hk, hv, heta, hW1, hW2, hW3 = pinned
     ws_host = torch.empty(cla.layer_host_workspace_size(B, H, N, d, m, b, cla.TTT_BF16, wl.mode,
-                                                        rule), device=dev, dtype=torch.uint8)
+                                                        step.rule), device=dev, dtype=torch.uint8)
 
     def e2e_step():
-        cla.ttt_layer_forward_host(hq, hk, hv, heta, hW1, hW2, hW3, b, wl.mode, rule, out=h_out,
-                                   W_final=h_W, workspace=ws_host)
+        cla.ttt_layer_forward_host(hq, hk, hv, heta, hW1, hW2, hW3, b, wl.mode, step.rule,
+                                   update_chunks=wl.update_chunks, out=h_out, W_final=h_W,
+                                   workspace=ws_host)
 
-    e2e_steps = max(1, min(args.steps, 10))
-    ms_e2e = time_steps(torch, e2e_step, e2e_steps, 1, stream)
-    max_e2e = reduce_max(ms_e2e, dev)
-    e2e_value = aggregate_throughput(tokens * e2e_steps, world, max_e2e / 1e3)
+    e2e_steps = max(1, min(args.steps, 20))
+    ms_e2e = time_steps(torch, e2e_step, e2e_steps, 3, stream)
+    check_status(cla)
+    e2e_value = tokens * e2e_steps / (ms_e2e / 1e3)
     h2d = sum(t.numel() * t.element_size() for t in pinned)
     d2h = h_out.numel() * h_out.element_size() + sum(t.numel() * t.element_size() for t in h_W)
+    del ws_host
 
     # per-launch profile of one more step (CUDA events around every launch)
     cla.profile_start()
     step()
     prof = cla.profile_stop()
-    tc_kernels = ("umma_gemm_kernel", "ns_cluster_kernel", "ns_panel_kernel", "ns_half_kernel")
+    check_status(cla)
+    tc_kernels = ("umma_gemm_kernel", "ns_cluster_kernel", "ns_half_kernel")
     gemm = [p for p in prof if p["kernel"] in tc_kernels]
     g_fl = sum(p["flops"] for p in gemm)
     g_n = sum(p["launches"] for p in gemm)
@@ -424,7 +525,6 @@ def run_ours(args):
         k_["flops"] += p["flops"]
         k_["sm_ms"] += p.get("sm_ms", p["ms"])
     dom_name, dom = max(per_kernel.items(), key=lambda kv: kv[1]["sm_ms"])
-    peaks, peak_src = load_peaks()
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     flops_step = layer_flops(wl)
@@ -434,98 +534,83 @@ def run_ours(args):
     # tensor-core kernels' achieved rate is their algorithmic FLOPs (which
     # are all of the step's FLOPs) over the timed step.
     achieved = g_fl / (ms_step / 1e3) / 1e12
+    q_bytes = 3 * inputs[0].numel() * inputs[0].element_size()
+    del step, inputs
+    torch.cuda.empty_cache()
 
-    # chunked linear attention (the linear-fast-weight reduction), HBM-bound
     lin = None
-    if rank == 0 and not args.skip_linattn:
-        lw = workloads.LINATTN_C2
-        lq, lk, lv, leta, _ = [t.to(dev) if t is not None else None
-                               for t in workloads.linattn_inputs(lw)]
-        lo = torch.empty_like(lq)
-        lS = torch.empty((lw.B, lw.H, lw.d_v, lw.d_k), device=dev)
-        lws = torch.empty(cla.linattn_workspace_size(lw.B, lw.H, lw.N, lw.d_k, lw.d_v, lw.chunk,
-                                                     cla.TTT_BF16, lw.mode),
-                          device=dev, dtype=torch.uint8)
-        lstep = lambda: cla.linattn_chunked_forward(lq, lk, lv, leta, lw.chunk, lw.mode, out=lo,
-                                                    S_final=lS, workspace=lws)
-        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-        tot = 0.0
-        reps = 20
-        for i in range(reps + 3):
-            flush.zero_()    # evict the inputs from L2 between repetitions
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            lstep()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            if i >= 3:
-                tot += e0.elapsed_time(e1)
-        lms = tot / reps
-        io_bytes = (3 * lq.numel() * 2 + leta.numel() * 4 + lo.numel() * 2)
-        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-        lin = {"workload": lw.name, "us_per_call": lms * 1e3,
-               "tokens_per_s": lw.B * lw.N / (lms / 1e3),
-               "gbs": io_bytes / (lms / 1e3) / 1e9, "hbm_frac": io_bytes / (lms / 1e3) / 1e9 / hbm,
-               "io_bytes": io_bytes, "l2": "flushed (256 MB write) before each call"}
+    if not args.skip_linattn:
+        lin = time_linattn(torch, cla, dev, stream, peaks)
+
+    extra = {}
+    if not args.skip_workloads:
+        for key in WORKLOADS:
+            if key == args.workload:
+                continue
+            ew = workload_by_key(key)
+            big = ew.B * ew.H * ew.N * ew.d_h > HOST_DRAW_LIMIT
+            extra[key] = time_extra_workload(torch, cla, ew, dev, stream, peaks,
+                                             steps=5 if big else 20, warmup=3)
 
     cpu = None
-    if rank == 0 and not args.skip_cpu_baseline:
-        rate, desc, _ = oracle_sample(wl, host, budget_s=args.ref_budget)
+    if not args.skip_cpu_baseline:
+        rate, desc, _ = oracle_sample(wl, budget_s=args.ref_budget)
         cpu = {"value": rate, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                "sample": desc}
 
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic",
-            "config": {"workload": wl.name, "B": B, "H": H, "N": N, "d_h": d, "m_h": m,
-                       "chunk": b, "mask": "apply-then-update", "muon_steps": wl.muon_steps,
-                       "momentum_beta": wl.momentum_beta, "l2norm": wl.l2norm,
-                       "io": "bf16 q/k/v, fp32 eta and fast weights",
-                       "l2": "inputs larger than L2 (q, k, v: %.0f MB per step)"
-                             % (3 * q.numel() * 2 / 1e6),
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
-            "pct_bf16_peak": {"step_tflops": step_tflops, "frac_of_burst": step_tflops / peak_burst,
-                              "frac_of_sustained": step_tflops / peak_sus,
-                              "flops_per_step": flops_step, "peaks": peak_src},
-            "roofline": roofline_entry(dom_name, dom, peak_sus, peak_src),
-            "tensor_kernels": {"launches_per_step": g_n, "flops_per_step": g_fl,
-                               "achieved_tflops_over_step": achieved,
-                               "note": "all tensor-core launches' algorithmic FLOPs over the "
-                                       "step time (stream groups overlap)"},
-            "breakdown_note": "summed launch durations of one profiled step; launches of "
-                              "different sequences overlap, so sums exceed the step time",
-            "breakdown": {p["name"]: {"launches": p["launches"], "ms": p["ms"],
-                                      "gpu_ms": p.get("sm_ms"),
-                                      "tflops": p["flops"] / (p["ms"] / 1e3) / 1e12
-                                      if p["flops"] and p["ms"] else None,
-                                      "gbs": p["bytes"] / (p["ms"] / 1e3) / 1e9
-                                      if p["bytes"] and p["ms"] else None}
-                          for p in prof},
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": max_e2e / e2e_steps},
-            "cpu_baseline": cpu,
-            "gpu_launches": launches,
-            "clocks": clk,
-            "linattn": lin,
-        }
-        print(json.dumps(line), flush=True)
+    cfg = workload_config(wl)
+    cfg.update({"io": "bf16 q/k/v, fp32 eta and fast weights",
+                "l2": "inputs larger than L2 (q, k, v: %.0f MB per step)" % (q_bytes / 1e6),
+                "parallelism": "single GPU"})
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": cfg,
+        "pct_bf16_peak": {"step_tflops": step_tflops, "frac_of_burst": step_tflops / peak_burst,
+                          "frac_of_sustained": step_tflops / peak_sus,
+                          "flops_per_step": flops_step, "peaks": peak_src},
+        "roofline": roofline_entry(dom_name, dom, peak_sus, peak_src),
+        "tensor_kernels": {"launches_per_step": g_n, "flops_per_step": g_fl,
+                           "achieved_tflops_over_step": achieved,
+                           "note": "all tensor-core launches' algorithmic FLOPs over the "
+                                   "step time (stream groups overlap)"},
+        "breakdown_note": "summed launch durations of one profiled step; launches of "
+                          "different sequences overlap, so sums exceed the step time",
+        "breakdown": {p["name"]: {"launches": p["launches"], "ms": p["ms"],
+                                  "gpu_ms": p.get("sm_ms"),
+                                  "tflops": p["flops"] / (p["ms"] / 1e3) / 1e12
+                                  if p["flops"] and p["ms"] else None,
+                                  "gbs": p["bytes"] / (p["ms"] / 1e3) / 1e9
+                                  if p["bytes"] and p["ms"] else None}
+                      for p in prof},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e / e2e_steps,
+                "steps": e2e_steps},
+        "cpu_baseline": cpu,
+        "gpu_launches": launches,
+        "clocks": clk,
+        "linattn": lin,
+        "workloads": extra,
+    }
+    print(json.dumps(line), flush=True)
     return 0
 
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=WORKLOADS, default=WORKLOADS[0],
+                    help="the workload of the headline figure")
     ap.add_argument("--ref-budget", type=float, default=12.0,
                     help="seconds of oracle work per CPU-baseline sample")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-linattn", action="store_true")
+    ap.add_argument("--skip-workloads", action="store_true",
+                    help="time only the headline workload")
     ap.add_argument("--seq-len", type=int, default=None,
                     help="override the workload's sequence length (small profiling cases)")
     args = ap.parse_args(argv)

@@ -33,7 +33,7 @@ EXPORTED = (
     "linattn_workspace_size", "linattn_chunked_forward", "ttt_device_status",
     "ttt_set_wait_limit_ns", "ttt_selftest_gemm", "ttt_launch_count", "ttt_profile_start",
     "ttt_profile_stop", "linattn_chunked_forward_noalloc", "ttt_layer_host_workspace_size",
-    "ttt_layer_forward_host",
+    "ttt_layer_forward_host", "ttt_selftest_withhold_release",
 )
 
 
@@ -96,6 +96,8 @@ def _declare(lib):
     lib.linattn_chunked_forward_noalloc.restype = i
     lib.linattn_chunked_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i,
                                                     vp, vp, vp, vp]
+    lib.ttt_selftest_withhold_release.restype = None
+    lib.ttt_selftest_withhold_release.argtypes = [i]
     lib.ttt_launch_count.restype = ctypes.c_ulonglong
     lib.ttt_launch_count.argtypes = []
     lib.ttt_profile_start.restype = None
@@ -320,9 +322,13 @@ def linattn_chunked_forward_noalloc(q, k, v, eta, chunk: int, mask_mode: int,
     if S_final is None:
         S_final = torch.empty((B, H, dv, dk), device=dev, dtype=torch.float32)
     keep, fl = _flags(update_chunks, N // chunk if chunk > 0 else 0)
-    rc = lib.linattn_chunked_forward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(eta), _ptr(S0), B, H,
-                                             N, dk, dv, chunk, _io_dtype(q), mask_mode, fl,
-                                             _ptr(out), _ptr(S_final), _stream(stream))
+    # the library looks up its scratch array on the CURRENT device: make it
+    # the tensors' device for the call
+    with torch.cuda.device(dev):
+        rc = lib.linattn_chunked_forward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(eta), _ptr(S0),
+                                                 B, H, N, dk, dv, chunk, _io_dtype(q), mask_mode,
+                                                 fl, _ptr(out), _ptr(S_final),
+                                                 _stream(stream))
     del keep
     _check(rc, "linattn_chunked_forward_noalloc")
     return out, S_final
@@ -354,6 +360,13 @@ def profile_stop():
 
 def set_wait_limit_ns(ns: int):
     library().ttt_set_wait_limit_ns(int(ns))
+
+
+def selftest_withhold_release(bh: int):
+    """Test hook: from the next linear-attention call on, batch-head ``bh``'s
+    state items never report completion, so the items waiting for them run
+    into their bounded waits (-1 turns it off).  See include/ttt_selftest.h."""
+    library().ttt_selftest_withhold_release(int(bh))
 
 
 def selftest_gemm(A, B, a_mn_major: bool, b_mn_major: bool, tile_n: int = 128, stream=None):

@@ -2,10 +2,12 @@
 // is enqueued), the device status word, and dispatch to the orchestration.
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "ttt.h"
 #include "ttt_selftest.h"
 #include "layer.h"
+#include "linattn_fused.h"
 
 namespace {
 
@@ -15,11 +17,13 @@ unsigned long long g_wait_limit_ns = 2000000000ull;
 
 constexpr int kMaxDevices = 64;
 int* g_status_ptr[kMaxDevices] = {nullptr};
+std::mutex g_status_mu;
 
 // Device address of the status word for the current device (looked up once).
 int* status_ptr() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_status_mu);
   if (!g_status_ptr[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_ttt_status) != cudaSuccess) return nullptr;
@@ -316,5 +320,7 @@ int ttt_selftest_gemm(const void* A, const void* B, float* D, int Z, int M, int 
                             dtype == TTT_BF16, tile_n, reinterpret_cast<cudaStream_t>(stream), st,
                             g_wait_limit_ns);
 }
+
+void ttt_selftest_withhold_release(int bh) { ttt::linattn_fused_withhold_release(bh); }
 
 }  // extern "C"

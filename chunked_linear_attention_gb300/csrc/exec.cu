@@ -51,15 +51,19 @@ bool ensure_events(DevicePool* p, size_t n) {
 }
 
 bool graphs_disabled() {
-  static int v = -1;
-  if (v < 0) {
+  static const bool v = [] {
     const char* s = std::getenv("TTT_DISABLE_GRAPHS");
-    v = (s && s[0] && s[0] != '0') ? 1 : 0;
-  }
-  return v == 1;
+    return s && s[0] && s[0] != '0';
+  }();
+  return v;
 }
 
 }  // namespace
+
+std::mutex& setup_mutex() {
+  static std::mutex mu;
+  return mu;
+}
 
 bool stream_pool(int n, std::vector<cudaStream_t>* out) {
   if (n > kMaxPool) return false;

@@ -9,9 +9,15 @@
 
 #include <cstdint>
 #include <functional>
+#include <mutex>
 #include <vector>
 
 namespace ttt {
+
+// Guards the one-time, per-device setup caches of the kernels (function
+// attributes, occupancy checks, SM counts): two host threads making their
+// first call at the same time fill each cache once.
+std::mutex& setup_mutex();
 
 // Internal non-blocking streams of the current device (created on first use).
 // Returns false if the pool cannot provide `n` streams.

@@ -10,6 +10,7 @@
 // double-buffered, so the epilogue of one tile overlaps the MMAs of the next;
 // the producer always runs ahead into the next tile.  Every wait is bounded
 // and reports TTT_ERR_TIMEOUT into the device status word.
+#include "exec.h"
 #include "launch.h"
 #include "tc_epilogue.cuh"
 #include "umma_core.cuh"
@@ -180,6 +181,7 @@ cudaError_t prepare_umma_gemm() {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(setup_mutex());
   if (!g_attr_done[dev]) {
     e = cudaFuncSetAttribute(umma_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kUmmaSmemBytes);

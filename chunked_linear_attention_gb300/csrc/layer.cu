@@ -36,30 +36,23 @@
 #include "exec.h"
 #include "ns_cluster.h"
 #include "ns_half.h"
-#include "ns_panel.h"
 #include "prof.h"
 
 namespace ttt {
 
 namespace {
 
-// Newton-Schulz kernel choice for square d x d matrices: the half-panel
-// kernel (d % 128 == 0, d <= 512) by default, the row-panel kernel
-// (d <= 384) with TTT_NS_KERNEL=panel, the tile-cluster kernel with
-// TTT_NS_KERNEL=cluster or when neither applies.
-int ns_kernel_choice() {
-  static int v = -1;
-  if (v < 0) {
-    const char* s = std::getenv("TTT_NS_KERNEL");
-    v = 0;
-    if (s && std::strcmp(s, "panel") == 0) v = 1;
-    if (s && std::strcmp(s, "cluster") == 0) v = 2;
-  }
-  return v;
-}
-bool use_ns_half(int d) { return ns_kernel_choice() == 0 && ns_half_applicable(d); }
-bool use_ns_panel(int d) { return ns_kernel_choice() == 1 && ns_panel_applicable(d); }
+// Newton-Schulz kernel for square d x d matrices: the half-panel kernel
+// (d % 128 == 0, d <= 512), else the tile-cluster kernel (other square
+// d <= 512), else the per-product GEMM launches.
+bool use_ns_half(int d) { return ns_half_applicable(d); }
 
+// An integer environment knob, read once (thread-safe: function-local statics
+// are initialised exactly once).  `dflt` when unset or empty.
+int env_int(const char* name, int dflt) {
+  const char* s = std::getenv(name);
+  return (s && s[0]) ? std::atoi(s) : dflt;
+}
 
 constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -200,12 +193,7 @@ struct IoHooks {
 // keep taking about as long, and as 15 / steps with fewer Muon steps, as the
 // chain then gets shorter (only that layer and 5 steps measured).
 int apply_ctas(int nh, int muon_steps, const LayerDims& D) {
-  static int v = -1;
-  if (v < 0) {
-    const char* s = std::getenv("TTT_APPLY_CTAS");
-    v = (s && s[0]) ? std::atoi(s) : 0;
-    if (v < 0) v = 0;
-  }
+  static const int v = std::max(0, env_int("TTT_APPLY_CTAS", 0));
   const double work = (double)D.chunk * D.d * D.m / (2048.0 * 384.0 * 384.0);
   const double per = v > 0 ? (double)v : 15.0 / muon_steps * (work > 1.0 ? work : 1.0);
   return (int)std::ceil(per * nh);
@@ -215,22 +203,14 @@ int apply_ctas(int nh, int muon_steps, const LayerDims& D) {
 // launches (TTT_GEMM_PRIORITY_OFFSET=k: k levels; measured on the 760M-scale
 // layer: 0, 1, 2 -> 2.92, 2.90, 2.91 ms per step).
 int gemm_priority_offset() {
-  static int v = -1;
-  if (v < 0) {
-    const char* s = std::getenv("TTT_GEMM_PRIORITY_OFFSET");
-    v = (s && s[0]) ? std::max(0, std::atoi(s)) : 1;
-  }
+  static const int v = std::max(0, env_int("TTT_GEMM_PRIORITY_OFFSET", 1));
   return v;
 }
 
 // TTT_CHAIN_PRIORITY=0 launches the update chain at the streams' own priority.
 bool chain_priority_on() {
-  static int v = -1;
-  if (v < 0) {
-    const char* s = std::getenv("TTT_CHAIN_PRIORITY");
-    v = (s && s[0] == '0') ? 0 : 1;
-  }
-  return v == 1;
+  static const bool v = env_int("TTT_CHAIN_PRIORITY", 1) != 0;
+  return v;
 }
 
 // The apply side of a step (query projections and the output GEMM of its
@@ -246,10 +226,8 @@ struct ApplyEvents {
   cudaEvent_t ev_a[2];
 };
 
-// `after_first`: if set, recorded on `st` once the first step's projection and
-// gradient launches are enqueued (stream groups start staggered on it).
 int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStream_t st,
-                  cudaEvent_t after_first = nullptr, const IoHooks* io = nullptr,
+                  const IoHooks* io = nullptr,
                   cudaStream_t sa = nullptr, const ApplyEvents* aev = nullptr) {
   const LayerArgs& a = *L.a;
   const LayerDims& D = *L.D;
@@ -414,10 +392,6 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
       const int rc = copy_out(ap, st);
       if (rc != 0) return rc;
     }
-    if (after_first) {
-      TTT_CK(cudaEventRecord(after_first, st));
-      after_first = nullptr;
-    }
 
     if (up < 0) continue;
 
@@ -455,7 +429,6 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
       na.priority = prio;
       int rc = 1;
       if (use_ns_half(d)) rc = launch_ns_half(cache, na, L.status, L.wait_ns, st);
-      if (rc == 1 && use_ns_panel(d)) rc = launch_ns_panel(cache, na, L.status, L.wait_ns, st);
       if (rc == 1) {
         TTT_CK(launch_normsq_reduce(w.normsq_part, w.nslot, w.normsq, BH, h0, nh, st));
         rc = launch_ns_cluster(cache, na, L.status, L.wait_ns, st);
@@ -592,31 +565,14 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
 bool per_sequence_streams(const LayerDims& D) {
   if (!D.bf16 || D.B * D.H < 2) return false;
   if (D.muon_steps == 0) return true;
-  return D.d == D.m && ((use_ns_half(D.d) && prepare_ns_half(D.d)) ||
-                        (use_ns_panel(D.d) && prepare_ns_panel(D.d)) || prepare_ns_cluster(D.d));
+  return D.d == D.m && ((use_ns_half(D.d) && prepare_ns_half(D.d)) || prepare_ns_cluster(D.d));
 }
 
 // The apply side of every step runs on its own stream per group (bf16 path);
 // TTT_SPLIT_APPLY=0 keeps it in the update chain's launches instead.
 bool split_apply_on() {
-  static int v = -1;
-  if (v < 0) {
-    const char* s = std::getenv("TTT_SPLIT_APPLY");
-    v = (s && s[0] == '0') ? 0 : 1;
-  }
-  return v == 1;
-}
-
-// TTT_STAGGER=1 starts stream group g only after group g-1's first
-// projections and gradients (default: all groups start together, measured
-// slightly faster with the half-panel Newton-Schulz kernel).
-bool stagger_on() {
-  static int v = -1;
-  if (v < 0) {
-    const char* s = std::getenv("TTT_STAGGER");
-    v = (s && s[0] == '1') ? 1 : 0;
-  }
-  return v == 1;
+  static const bool v = env_int("TTT_SPLIT_APPLY", 1) != 0;
+  return v;
 }
 
 // Number of stream groups the (batch, head) sequences are split into: each
@@ -632,11 +588,7 @@ bool stagger_on() {
 int sequence_groups(const LayerDims& D, bool split) {
   const int BH = D.B * D.H;
   if (!per_sequence_streams(D)) return 1;
-  static int env = -2;
-  if (env == -2) {
-    const char* s = std::getenv("TTT_SEQUENCE_GROUPS");
-    env = (s && s[0]) ? std::atoi(s) : -1;
-  }
+  static const int env = env_int("TTT_SEQUENCE_GROUPS", -1);
   if (env >= 1) return env < BH ? env : BH;
   const int def = split ? 4 : (D.muon_steps > 0 ? 3 : 1);
   return BH < def ? BH : def;
@@ -679,7 +631,7 @@ int enqueue_all(LayerPlan& L, cudaStream_t st) {
   // streams: [0, ng) compute groups when ng > 1, then one apply stream per
   // group (bf16 device-buffer calls), then for host-buffer calls one
   // host-to-device stream and one device-to-host stream per group.  Events per
-  // group: stagger, ev_w, ev_a[2].  Host-buffer calls keep the apply side in
+  // group: ev_w and ev_a[2] (the group's first event is spare).  Host-buffer calls keep the apply side in
   // the chain's launches: with the extra streams their input copies stalled
   // behind queued kernels (8-9 ms per call instead of 4.7 ms).  Without Muon
   // the update chain is short and the capped apply side would set the pace
@@ -743,20 +695,17 @@ int enqueue_all(LayerPlan& L, cudaStream_t st) {
   if (ng > 1) {
     std::vector<cudaStream_t> kids(pool.begin(), pool.begin() + ng);
     TTT_CK(fork_streams(st, kids));
-    // Group g covers a contiguous range of sequences on its own stream; with
-    // TTT_STAGGER=1 it starts once group g-1 has its first projections and
-    // gradients enqueued.
+    // Group g covers a contiguous range of sequences on its own stream.
     for (int g = 0; g < ng; ++g) {
       const int h0 = (int)((long long)BH * g / ng), h1 = (int)((long long)BH * (g + 1) / ng);
-      if (g > 0 && stagger_on()) TTT_CK(cudaStreamWaitEvent(kids[g], sev[4 * (g - 1)], 0));
-      const int rc = enqueue_range(L, cache, h0, h1 - h0, kids[g], sev[4 * g],
-                                   hio ? &hooks[g] : nullptr, split ? pool[ap0 + g] : nullptr,
+      const int rc = enqueue_range(L, cache, h0, h1 - h0, kids[g], hio ? &hooks[g] : nullptr,
+                                   split ? pool[ap0 + g] : nullptr,
                                    split ? &aevs[g] : nullptr);
       if (rc != 0) return rc;
     }
     TTT_CK(join_streams(st, kids));
   } else {
-    const int rc = enqueue_range(L, cache, 0, BH, st, nullptr, hio ? &hooks[0] : nullptr,
+    const int rc = enqueue_range(L, cache, 0, BH, st, hio ? &hooks[0] : nullptr,
                                  split ? pool[ap0] : nullptr, split ? &aevs[0] : nullptr);
     if (rc != 0) return rc;
   }
@@ -873,7 +822,6 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
     if (prepare_umma_gemm() != cudaSuccess) return -6;
     if (muon && d == m) {
       if (use_ns_half(d)) prepare_ns_half(d);
-      if (use_ns_panel(d)) prepare_ns_panel(d);
       prepare_ns_cluster(d);
     }
   }

@@ -28,10 +28,12 @@
 // MMAs, warps 2..5 scale, drain TMEM (warp w reads lanes 32 (w % 4) ..) and
 // run the prefix items.  Every mbarrier and counter wait is bounded and
 // reports TTT_ERR_TIMEOUT.
+#include <atomic>
 #include <cstring>
 
 #include "builder.h"
 #include "common.cuh"
+#include "exec.h"
 #include "launch.h"
 #include "linattn_fused.h"
 #include "prof.h"
@@ -65,6 +67,7 @@ struct LinFusedLaunch {
   UpdateFlags flags;
   int* status;
   unsigned long long wait_limit_ns;
+  int withhold_bh;            // test hook: this batch-head's A items never release (-1: none)
 };
 
 static_assert(sizeof(LinFusedLaunch) <= 4096, "kernel parameter block too large");
@@ -464,7 +467,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
         }
         ++u;
         named_bar_sync(1, 128);
-        if (tid == 0 && ok) {
+        if (tid == 0 && ok && it.bh != L.withhold_bh) {
           __threadfence();
           atomicAdd(doneA + it.bh, 1);
         }
@@ -527,8 +530,11 @@ __global__ void __launch_bounds__(kLThreads, 1)
 
 int g_fused_ready[64] = {0};   // 0 unknown, 1 usable, 2 not usable
 int g_fused_sms[64] = {0};
+std::atomic<int> g_withhold_bh{-1};
 
 }  // namespace
+
+void linattn_fused_withhold_release(int bh) { g_withhold_bh.store(bh < 0 ? -1 : bh); }
 
 bool linattn_fused_applicable(const LinDims& D) {
   if (!D.bf16) return false;
@@ -561,6 +567,7 @@ size_t linattn_fused_scratch(const LinDims& D, const LinFusedPlan& p) {
 bool prepare_linattn_fused() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lk(setup_mutex());
   int& r = g_fused_ready[dev];
   if (r == 0) {
     r = 2;
@@ -642,6 +649,7 @@ int launch_linattn_fused(MapCache& cache, const LinFusedArgs& a, int* status,
   L.nstages = nst;
   L.status = status;
   L.wait_limit_ns = wait_ns;
+  L.withhold_bh = g_withhold_bh.load();
 
   if (cudaMemsetAsync(L.counters, 0, 2 * (size_t)BH * sizeof(int), stream) != cudaSuccess)
     return -6;

@@ -28,6 +28,11 @@ struct LinFusedArgs {
   void* scratch;                // linattn_fused_scratch() bytes, 256-byte aligned
 };
 
+// Test hook: from the next launch on, batch-head `bh`'s state items never
+// report completion (-1 turns this off), so that the items waiting for them
+// run into their bounded waits.
+void linattn_fused_withhold_release(int bh);
+
 // True for the shapes the kernel handles: bf16, d_v = 128, d_k = 64 or 128,
 // chunk a multiple of 128.
 bool linattn_fused_applicable(const LinDims& D);

@@ -18,6 +18,7 @@
 #include <cstring>
 
 #include "builder.h"
+#include "exec.h"
 #include "launch.h"
 #include "ns_cluster.h"
 #include "prof.h"
@@ -262,6 +263,7 @@ bool ns_cluster_applicable(int d, int* cs_out, int* bn_out) {
 
 static bool cluster_fits(int dev, int cs) {
   if (dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lk(setup_mutex());
   int& c = cluster_ok_cache[dev][cs];
   if (c == 0) {
     c = 2;
@@ -339,6 +341,7 @@ int launch_ns_cluster(MapCache& cache, const NsArgs& a, int* status, unsigned lo
   auto op = [&](int map, int mn) {
     OpDesc o;
     std::memset(&o, 0, sizeof(o));
+    o.map3 = -1;   // MN-major tiles go as 64-column 2-D boxes (no 3-D map here)
     o.map = map;
     o.mn_major = mn;
     o.z_outer = d;

@@ -35,6 +35,7 @@
 
 #include "builder.h"
 #include "common.cuh"
+#include "exec.h"
 #include "launch.h"
 #include "ns_cluster.h"
 #include "ns_half.h"
@@ -505,6 +506,7 @@ bool prepare_ns_half(int d) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   const int cs = 2 * (d / 128);
+  std::lock_guard<std::mutex> lk(setup_mutex());
   int& c = g_half_fit[dev][cs];
   if (c == 0) {
     c = 2;

@@ -20,7 +20,6 @@ enum ProfTag : int {
   PT_LIN_OUT,
   PT_SELFTEST,
   PT_MUON,
-  PT_MUON_PANEL,
   PT_MUON_HALF,
   PT_LIN_FUSED,
   PT_APPLY_PROJ,

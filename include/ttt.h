@@ -210,9 +210,11 @@ int linattn_chunked_forward(const void* q, const void* k, const void* v, const f
  * workspace: the scratch comes from a fixed 16 MiB array in device memory
  * that every GPU loading the library reserves until the process exits.
  * Allocates nothing.  Problems whose linattn_workspace_size() exceeds 16 MiB
- * return TTT_ERR_WORKSPACE before anything is enqueued.  The first call on
- * each device looks up the array's device address with a runtime call (with
- * that device current), so make it before any stream capture begins.  All
+ * return TTT_ERR_WORKSPACE before anything is enqueued.  The array used is
+ * the CURRENT device's (cudaGetDevice), so the current device must be the
+ * device of `stream` and of every tensor.  The first call on each device
+ * looks up the array's device address with a runtime call (with that device
+ * current), so make it before any stream capture begins.  All
  * calls share the array: calls that overlap on the GPU (e.g. concurrently on
  * two streams) race on it and must be serialised by the caller. */
 int linattn_chunked_forward_noalloc(const void* q, const void* k, const void* v,

@@ -27,6 +27,18 @@ int ttt_selftest_gemm(const void* A, const void* B, float* D, int Z, int M, int 
                       int a_mn_major, int b_mn_major, int dtype, int tile_n,
                       ttt_stream_t stream);
 
+/* Test hook for the bounded waits of the one-launch linear-attention kernel
+ * (linattn_chunked_forward on the shapes it handles: bf16, d_v = 128,
+ * d_k in {64, 128}).  From the next call on, the partial-state items of
+ * batch-head index `bh` (b * H + h) never report that they are done, so the
+ * items that wait for them (that batch-head's prefix and output items) run
+ * into their wait limit, record TTT_ERR_TIMEOUT in the device status word
+ * and give up without storing anything; the other batch-heads are computed
+ * as usual.  The waits that run out are taken before the waiting item issues
+ * any copy, so nothing is in flight when it gives up.  bh < 0 turns the hook
+ * off.  Process-wide; not for production use. */
+void ttt_selftest_withhold_release(int bh);
+
 #ifdef __cplusplus
 }
 #endif

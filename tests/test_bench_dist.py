@@ -1,8 +1,10 @@
-"""Multi-rank plumbing of bench.py on CPU (gloo, world size 2): the barrier, the
-maximum over ranks used for the timed region, the whole-job throughput, and
-the reference arm's rank gating.  No GPU is used."""
+"""Process-layout logic of bench.py on CPU (no GPU is used): a job on more
+than one GPU is refused with one line from rank 0 and exit status 0 on every
+rank, the reference arm runs on rank 0 only, and the roofline object's
+arithmetic."""
+import json
 import os
-import socket
+import subprocess
 import sys
 
 import pytest
@@ -12,51 +14,38 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
-def _free_port():
-    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as s:
-        s.bind(("127.0.0.1", 0))
-        return s.getsockname()[1]
+def _run_rank(rank, world, extra):
+    env = dict(os.environ, RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
+               MASTER_ADDR="127.0.0.1", MASTER_PORT="29555", CUDA_VISIBLE_DEVICES="")
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *extra], env=env,
+                          capture_output=True, text=True, timeout=300, cwd=ROOT)
 
 
-def _rank_main(rank, world, port, out_dir):
-    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
-                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
-    sys.path.insert(0, ROOT)
+def test_two_rank_job_is_refused_on_every_rank():
+    """Two ranks launched as torchrun would (RANK / WORLD_SIZE set): rank 0
+    prints one refusal line, rank 1 prints nothing, both exit 0."""
+    procs = [_run_rank(r, 2, ["--gpus", "2", "--steps", "2", "--warmup", "3"]) for r in (0, 1)]
+    for p in procs:
+        assert p.returncode == 0, p.stderr
+    lines = [ln for ln in procs[0].stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["n_gpus"] == 2 and line["value"] is None
+    assert "single-GPU" in line["unavailable"]
+    assert procs[1].stdout.strip() == ""
+
+
+def test_gpus_flag_alone_is_refused(monkeypatch):
     import bench
-    import torch.distributed as dist
-    r, w = bench.init_dist("gloo")
-    bench.barrier()
-    # each rank "measured" a different time; the job time is the slowest rank's
-    m = bench.reduce_max(10.0 + 5.0 * r)
-    thr = bench.aggregate_throughput(1000.0, w, m / 1e3)
-    bench.barrier()
-    with open(os.path.join(out_dir, f"rank{rank}.txt"), "w") as f:
-        f.write(f"{r} {w} {m} {thr}\n")
-    dist.destroy_process_group()
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
 
+    class A:
+        gpus, steps, warmup = 4, 1, 3
 
-def test_reduce_max_and_throughput_two_ranks(tmp_path):
-    import torch.multiprocessing as mp
-    port = _free_port()
-    mp.start_processes(_rank_main, args=(2, port, str(tmp_path)), nprocs=2, join=True,
-                       start_method="spawn")
-    rows = []
-    for r in range(2):
-        with open(tmp_path / f"rank{r}.txt") as f:
-            rows.append(f.read().split())
-    for r, row in enumerate(rows):
-        rr, w, m, thr = int(row[0]), int(row[1]), float(row[2]), float(row[3])
-        assert rr == r and w == 2
-        assert m == pytest.approx(15.0)            # max over ranks, seen by every rank
-        # 1000 units per rank, 2 ranks, over the slowest rank's 15 ms
-        assert thr == pytest.approx(1000.0 * 2 / 0.015)
-
-
-def test_single_process_helpers_without_process_group():
-    import bench
-    assert bench.reduce_max(3.25) == 3.25
-    assert bench.aggregate_throughput(10.0, 1, 2.0) == 5.0
-    bench.barrier()   # no process group: a no-op
+    r = bench.single_gpu_refusal(A())
+    assert r is not None and r["n_gpus"] == 4
+    A.gpus = 1
+    assert bench.single_gpu_refusal(A()) is None
 
 
 def test_reference_arm_other_ranks_exit_without_work(monkeypatch, capsys):
@@ -65,10 +54,39 @@ def test_reference_arm_other_ranks_exit_without_work(monkeypatch, capsys):
     monkeypatch.setenv("WORLD_SIZE", "2")
 
     class A:
-        gpus, steps, warmup, ref_budget = 2, 1, 3, 0.1
+        gpus, steps, warmup, ref_budget, workload = 2, 1, 3, 0.1, "lm760m"
 
     assert bench.run_reference(A()) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_line_on_rank_zero(monkeypatch, capsys):
+    """Rank 0 of the reference arm prints one line with the oracle's rate
+    (a tiny budget: one run of the sampled chunks)."""
+    import bench
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+
+    class A:
+        gpus, steps, warmup, ref_budget, workload = 1, 1, 0, 0.01, "nvs-strided"
+
+    assert bench.run_reference(A()) == 0
+    line = json.loads(capsys.readouterr().out.strip())
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["config"]["update_chunks"] == [1, 1, 1, 1, 0, 0, 0, 0]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_layer_flops_per_workload():
+    """FLOP counts written out per workload: 18 b d m per chunk and head
+    (12 for an update, 6 for an apply) plus Muon's s (4 r c^2 + 2 c^3) per
+    matrix and update."""
+    import bench
+    import workloads as W
+    assert bench.layer_flops(W.LM_760M) == pytest.approx(1.348082860032e12)
+    # strided: 2 heads x (4 updates x 12 + 8 applies x 6) b d m
+    assert bench.layer_flops(W.NVS_STRIDED) == pytest.approx(2 * 96 * 8192 * 384 * 768)
+    assert bench.layer_flops(W.LONG_1M) == pytest.approx(25.98e12, rel=1e-3)
 
 
 def test_roofline_entry_per_launch_and_held_sm_rates():

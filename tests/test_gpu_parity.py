@@ -6,6 +6,8 @@ error (max|x - r| / max|r|) <= 1e-4 for the fp32 path; relative L2 error
 fast-weight matrix).
 """
 import dataclasses
+import json
+import os
 
 import numpy as np
 import pytest
@@ -132,6 +134,17 @@ BF16_CASES = [
     dict(mode=W.BLOCK_CAUSAL, chunk=256, N=512, d_h=512, m_h=512, muon_steps=2),
     dict(mode=W.APPLY_THEN_UPDATE, chunk=128, N=384, d_h=384, m_h=384, muon_steps=1,
          l2norm=False),
+    # square orders that are not multiples of 128: the tile-cluster Newton-Schulz
+    # kernel (clusters of 2, 6 and 8 CTAs).  With Muon, chunk >= d: a chunk
+    # shorter than d leaves the momentum rank-deficient, and each Newton-Schulz
+    # step multiplies its near-zero singular values by about a = 3.44, so bf16
+    # rounding noise there grows ~3.44^steps (rounding M alone to bf16 moves the
+    # oracle by 5e-2 at d = 320, chunk 128, 5 steps)
+    dict(mode=W.APPLY_THEN_UPDATE, chunk=128, N=512, d_h=192, m_h=192, muon_steps=3,
+         momentum_beta=0.9),
+    dict(mode=W.BLOCK_CAUSAL, chunk=384, N=768, d_h=320, m_h=320, muon_steps=3,
+         momentum_beta=0.9, l2_normed_k=True),
+    dict(mode=W.APPLY_THEN_UPDATE, chunk=256, N=512, d_h=448, m_h=448, muon_steps=2),
 ]
 
 
@@ -249,26 +262,92 @@ def test_linattn_full_size():
     assert rel_l2(f64(S), rS) <= BF16_REL_L2
 
 
-def test_layer_lm_full_size_sampled():
+GOLDEN_DRIFT = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                            "lm760m_drift.json")
+# The full-length bound: a chunk's error may be at most this multiple of what
+# rounding the oracle's own state to bf16 at every chunk boundary does to it
+# (tests/golden/lm760m_drift.json).  The bf16 path rounds more than the state
+# (GEMM operands, Newton-Schulz iterates, activations); it has measured about
+# 2-2.6 times that per-chunk injection.
+DRIFT_FACTOR = 4.0
+
+
+def test_layer_lm_full_size():
     """LM-style workload at full size (B2 H4 d=m=384 N32768 chunk 2048, Muon 5,
-    beta 0.9): the outputs of the first two chunks against the oracle's
-    prefix scan, the weights after two chunks from a prefix call, and unit
+    beta 0.9), every chunk against the oracle's full scan: chunks 0 and 1
+    within the bf16-with-Muon tolerance, every chunk and the final weights
+    within DRIFT_FACTOR times the oracle's own per-chunk sensitivity to bf16
+    rounding of its state (the scan amplifies any difference about 1.25x per
+    chunk, so the tolerance cannot hold at the end for a bf16 path); the
+    weights after two chunks from a prefix call within the tolerance; unit
     row norms of the final weights."""
     cla = lib()
     wl = W.LM_760M
     q, k, v, eta, W1, W2, W3 = W.layer_inputs(wl)
     got = run_layer(cla, wl, q, k, v, eta, W1, W2, W3)
-    nc = 2
-    pre = wl.chunk * nc
-    ref = run_oracle(wl, q, k, v, eta, W1, W2, W3, n_chunks=nc)
-    assert rel_l2(got[0][..., :pre, :], ref[0][..., :pre, :]) <= BF16_MUON_REL_L2
+    ref = run_oracle(wl, q, k, v, eta, W1, W2, W3)
+    with open(GOLDEN_DRIFT) as f:
+        drift = json.load(f)
+    b = wl.chunk
+    per = [rel_l2(got[0][..., c * b:(c + 1) * b, :], ref[0][..., c * b:(c + 1) * b, :])
+           for c in range(wl.N // b)]
+    wf = [rel_l2(got[i], ref[i]) for i in (1, 2, 3)]
+    print("per-chunk rel L2 vs oracle:", " ".join(f"{e:.2e}" for e in per))
+    print("per-chunk ratio to the state-rounding drift:",
+          " ".join(f"{e / d:.2f}" for e, d in zip(per, drift["per_chunk"])))
+    print("final weights rel L2:", wf)
+    assert per[0] <= BF16_MUON_REL_L2 and per[1] <= BF16_MUON_REL_L2, per
+    for c, (e, dr) in enumerate(zip(per, drift["per_chunk"])):
+        assert e <= DRIFT_FACTOR * dr, (c, e, dr)
+    for e, name in zip(wf, ("W1", "W2", "W3")):
+        assert e <= DRIFT_FACTOR * drift["final_weights"][name], (name, e)
     for Wf in got[1:]:
         np.testing.assert_allclose(np.linalg.norm(Wf, axis=-1), 1.0, atol=1e-3)
+    nc = 2
+    pre = wl.chunk * nc
+    refp = run_oracle(wl, q, k, v, eta, W1, W2, W3, n_chunks=nc)
     wp = dataclasses.replace(wl, N=pre)
     sl = lambda t: t[..., :pre, :].contiguous()
     gp = run_layer(cla, wp, sl(q), sl(k), sl(v), eta[..., :pre].contiguous(), W1, W2, W3)
-    errs = [rel_l2(g_, r_) for g_, r_ in zip(gp[1:], ref[1:4])]
+    errs = [rel_l2(g_, r_) for g_, r_ in zip(gp[1:], refp[1:4])]
     assert max(errs) <= BF16_MUON_REL_L2, errs
+
+
+def test_layer_long_context_prefix_and_full_length():
+    """Million-token workload (B1 H4 d=m=512, chunk 8192, Muon 5, beta 0.9):
+    a prefix call of its first three chunks (all four heads) against the
+    oracle, outputs and weights within the bf16-with-Muon tolerance; then the
+    full 1,048,576-token call, whose first three chunks hold the same inputs,
+    gives the same first-chunk outputs as the prefix call (the scan is causal)
+    and ends with unit-norm, finite weights."""
+    cla = lib()
+    wl = W.LONG_1M
+    nc = 3
+    pre = nc * wl.chunk
+    wp = dataclasses.replace(wl, N=pre)
+    q, k, v, eta, W1, W2, W3 = W.layer_inputs(wp)
+    gp = run_layer(cla, wp, q, k, v, eta, W1, W2, W3)
+    ref = run_oracle(wp, q, k, v, eta, W1, W2, W3)
+    errs = [rel_l2(g_, r_) for g_, r_ in zip(gp, ref[:4])]
+    print("long-context prefix rel L2 (out, W1, W2, W3):", errs)
+    assert max(errs) <= BF16_MUON_REL_L2, errs
+    fq, fk, fv, feta, _, _, _ = W.layer_inputs_on_device(wl, DEV, seed=1)
+    for dst, src in ((fq, q), (fk, k), (fv, v)):
+        dst[..., :pre, :] = src.to(DEV)
+    feta[..., :pre] = eta.to(DEV)
+    rule = cla.update_rule(l2norm=wl.l2norm, muon_steps=wl.muon_steps,
+                           momentum_beta=wl.momentum_beta)
+    out, F1, F2, F3 = cla.ttt_layer_forward(fq, fk, fv, feta, W1.to(DEV), W2.to(DEV), W3.to(DEV),
+                                            wl.chunk, wl.mode, rule)
+    torch.cuda.synchronize()
+    assert_status_ok(cla)
+    head = f64(out[..., :pre, :])
+    assert rel_l2(head, ref[0]) <= BF16_MUON_REL_L2
+    assert np.array_equal(head, gp[0])
+    for Wf in (F1, F2, F3):
+        n = torch.linalg.vector_norm(Wf, dim=-1)
+        assert bool(torch.isfinite(Wf).all())
+        assert float((n - 1).abs().max()) < 1e-3
 
 
 def test_layer_strided_full_size():

@@ -130,6 +130,37 @@ def layer_inputs(wl: LayerWorkload, B=None, H=None, N=None, seed=None):
             eta.contiguous(), W1, W2, W3)
 
 
+def layer_inputs_on_device(wl: LayerWorkload, device, seed=None):
+    """The layer workload's recipe drawn directly on a CUDA device (a seeded
+    CUDA generator, the same draw order and distributions as
+    ``layer_inputs``; the values differ from the CPU draw).  For workloads
+    too large to draw on the host in reasonable time (the million-token
+    context: 2^31 elements per tensor); used for timing only.
+    """
+    gen = torch.Generator(device=device)
+    gen.manual_seed(wl.seed if seed is None else seed)
+    d, m, B, H, N = wl.d_h, wl.m_h, wl.B, wl.H, wl.N
+    std = 1.0 / math.sqrt(d)
+    dt = torch.bfloat16 if wl.io_dtype == "bf16" else torch.float32
+
+    def io(shape):
+        x = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+        x.mul_(std)
+        return x.to(dt)
+
+    q = io((B, H, N, d))
+    k = io((B, H, N, d))
+    if wl.l2_normed_k:
+        raise ValueError("draw L2-normalised keys with layer_inputs")
+    v = io((B, H, N, d))
+    eta = torch.nn.functional.softplus(
+        torch.randn((B, H, N), generator=gen, device=device)) / wl.chunk
+    W1 = torch.randn((H, m, d), generator=gen, device=device) * std
+    W2 = torch.randn((H, d, m), generator=gen, device=device) * std
+    W3 = torch.randn((H, m, d), generator=gen, device=device) * std
+    return q, k, v, eta.contiguous(), W1, W2, W3
+
+
 def linattn_inputs(wl: LinattnWorkload, B=None, H=None, N=None, seed=None,
                    with_state=False):
     """Draw (q, k, v, eta, S0) on the CPU for a linear-attention workload.
