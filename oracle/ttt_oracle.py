@@ -339,3 +339,68 @@ def linattn_chunked_forward(q, k, v, eta, S0, chunk, mode, update_chunks=None):
                     out[b, h, sl] = q[b, h, sl] @ S.T
             Sf[b, h] = S
     return out, Sf
+
+
+# ---------------------------------------------------------------------------
+# chunked linear attention with momentum, a per-chunk learning rate and an
+# optional Muon of the momentum (the reducible TTT variants)
+
+def linattn_momentum_forward(q, k, v, eta, S0, chunk, mode, update_chunks=None,
+                             alpha=None, lr=None, M0=None, muon_steps=0,
+                             ns_coef=MUON_COEF):
+    """Chunked linear attention whose state is updated through a momentum
+    accumulator, with a per-chunk momentum coefficient and learning rate.
+
+    Follows the sequential recurrence of "Test-Time Training with KV Binding
+    Is Secretly Linear Attention": Thm 5.3 / App. D (gradient descent with a
+    per-step momentum factor alpha_t), App. H.2 (its chunk form with a
+    per-chunk learning rate), and App. E.3 (Muon applied to the momentum
+    accumulator).  With a linear fast weight f_S(x) = S x and the dot-product
+    loss the chunk's negative gradient is G_t = (eta * V_t)^T K_t (per-token
+    eta folded into the values), and per updating chunk t
+
+        M_t = alpha_t M_{t-1} + G_t          (M_{-1} = M0, zeros if None)
+        U_t = Muon(M_t) if muon_steps else M_t
+        S  <- S + lr_t U_t
+
+    Chunks that do not update (strided mask) leave M and S unchanged.  The
+    outputs O_t = Q_t S^T read S before (apply-then-update) or after the
+    chunk's update, as in linattn_chunked_forward.
+
+    q, k: [B, H, N, d_k]; v: [B, H, N, d_v]; eta: [B, H, N];
+    S0, M0: [B, H, d_v, d_k] or None; alpha, lr: [B, H, N / chunk] or None
+    (None: alpha = 0, i.e. no momentum; lr = 1).
+    Returns (out [B, H, N, d_v], S_final, M_final).
+    """
+    q, k, v, eta = _f64(q), _f64(k), _f64(v), _f64(eta)
+    B, H, N, dk = q.shape
+    dv = v.shape[-1]
+    if N % chunk != 0:
+        raise ValueError("sequence length must be a multiple of the chunk")
+    n = N // chunk
+    if mode == BIDIRECTIONAL and n != 1:
+        raise ValueError("bidirectional mode is a single chunk covering the sequence")
+    flags = _update_flags(n, mode, update_chunks)
+    al = np.zeros((B, H, n)) if alpha is None else _f64(alpha)
+    lrs = np.ones((B, H, n)) if lr is None else _f64(lr)
+    out = np.zeros((B, H, N, dv))
+    Sf = np.zeros((B, H, dv, dk))
+    Mf = np.zeros((B, H, dv, dk))
+    for b in range(B):
+        for h in range(H):
+            S = np.zeros((dv, dk)) if S0 is None else _f64(S0)[b, h].copy()
+            M = np.zeros((dv, dk)) if M0 is None else _f64(M0)[b, h].copy()
+            for c in range(n):
+                sl = slice(c * chunk, (c + 1) * chunk)
+                if mode == APPLY_THEN_UPDATE:
+                    out[b, h, sl] = q[b, h, sl] @ S.T
+                if flags[c]:
+                    G = (eta[b, h, sl, None] * v[b, h, sl]).T @ k[b, h, sl]
+                    M = al[b, h, c] * M + G
+                    U = newton_schulz(M, muon_steps, ns_coef) if muon_steps > 0 else M
+                    S = S + lrs[b, h, c] * U
+                if mode != APPLY_THEN_UPDATE:
+                    out[b, h, sl] = q[b, h, sl] @ S.T
+            Sf[b, h] = S
+            Mf[b, h] = M
+    return out, Sf, Mf
