@@ -33,7 +33,8 @@ EXPORTED = (
     "linattn_workspace_size", "linattn_chunked_forward", "ttt_device_status",
     "ttt_set_wait_limit_ns", "ttt_selftest_gemm", "ttt_launch_count", "ttt_profile_start",
     "ttt_profile_stop", "linattn_chunked_forward_noalloc", "ttt_layer_host_workspace_size",
-    "ttt_layer_forward_host", "ttt_selftest_withhold_release",
+    "ttt_layer_forward_host", "ttt_selftest_withhold_release", "linattn_rule_workspace_size",
+    "linattn_chunked_forward_rule",
 )
 
 
@@ -50,6 +51,13 @@ class UpdateRule(ctypes.Structure):
     _fields_ = [("l2norm", ctypes.c_int), ("muon_steps", ctypes.c_int),
                 ("momentum_beta", ctypes.c_float), ("ns_a", ctypes.c_float),
                 ("ns_b", ctypes.c_float), ("ns_c", ctypes.c_float)]
+
+
+class LinattnRule(ctypes.Structure):
+    """Mirror of ``linattn_rule``."""
+    _fields_ = [("alpha", ctypes.c_void_p), ("lr", ctypes.c_void_p), ("M0", ctypes.c_void_p),
+                ("M_final", ctypes.c_void_p), ("muon_steps", ctypes.c_int),
+                ("ns_a", ctypes.c_float), ("ns_b", ctypes.c_float), ("ns_c", ctypes.c_float)]
 
 
 def update_rule(l2norm=True, muon_steps=0, momentum_beta=0.0, ns_coef=MUON_COEF) -> UpdateRule:
@@ -87,6 +95,12 @@ def _declare(lib):
     lib.linattn_chunked_forward.restype = i
     lib.linattn_chunked_forward.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, vp,
                                             vp, vp, vp, sz, vp]
+    lib.linattn_rule_workspace_size.restype = sz
+    lib.linattn_rule_workspace_size.argtypes = [i, i, i, i, i, i, i, i,
+                                                ctypes.POINTER(LinattnRule)]
+    lib.linattn_chunked_forward_rule.restype = i
+    lib.linattn_chunked_forward_rule.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, vp,
+                                                 ctypes.POINTER(LinattnRule), vp, vp, vp, sz, vp]
     lib.ttt_device_status.restype = i
     lib.ttt_device_status.argtypes = [vp]
     lib.ttt_set_wait_limit_ns.restype = None
@@ -302,6 +316,56 @@ def linattn_chunked_forward(q, k, v, eta, chunk: int, mask_mode: int,
     del keep
     _check(rc, "linattn_chunked_forward")
     return out, S_final
+
+
+def linattn_rule(alpha=None, lr=None, M0=None, M_final=None, muon_steps=0,
+                 ns_coef=MUON_COEF) -> LinattnRule:
+    """The ``linattn_rule`` struct from CUDA tensors (or None)."""
+    a, b, c = ns_coef
+    return LinattnRule(_ptr(alpha), _ptr(lr), _ptr(M0), _ptr(M_final), int(muon_steps),
+                       float(a), float(b), float(c))
+
+
+def linattn_chunked_forward_rule(q, k, v, eta, chunk: int, mask_mode: int,
+                                 S0: Optional[torch.Tensor] = None,
+                                 update_chunks: Optional[Sequence[int]] = None,
+                                 alpha: Optional[torch.Tensor] = None,
+                                 lr: Optional[torch.Tensor] = None,
+                                 M0: Optional[torch.Tensor] = None,
+                                 M_final=None, muon_steps: int = 0, ns_coef=MUON_COEF,
+                                 out: Optional[torch.Tensor] = None,
+                                 S_final: Optional[torch.Tensor] = None,
+                                 workspace: Optional[torch.Tensor] = None, stream=None):
+    """Chunked linear attention with momentum, per-chunk learning rates and
+    Muon of the momentum (see ``linattn_chunked_forward_rule`` in
+    include/ttt.h).  alpha, lr: [B, H, N / chunk] fp32 CUDA tensors or None;
+    M0 [B, H, d_v, d_k] or None; M_final: a tensor to write, True to allocate
+    one, or None.  Returns (out, S_final, M_final or None)."""
+    lib = library()
+    B, H, N, dk = q.shape
+    dv = v.shape[-1]
+    io = _io_dtype(q)
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, H, N, dv), device=dev, dtype=q.dtype)
+    if S_final is None:
+        S_final = torch.empty((B, H, dv, dk), device=dev, dtype=torch.float32)
+    if M_final is True:
+        M_final = torch.empty((B, H, dv, dk), device=dev, dtype=torch.float32)
+    rule = linattn_rule(alpha, lr, M0, M_final, muon_steps, ns_coef)
+    ws_bytes = lib.linattn_rule_workspace_size(B, H, N, dk, dv, chunk, io, mask_mode,
+                                               ctypes.byref(rule))
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
+    keep, fl = _flags(update_chunks, N // chunk if chunk > 0 else 0)
+    rc = lib.linattn_chunked_forward_rule(_ptr(q), _ptr(k), _ptr(v), _ptr(eta), _ptr(S0), B, H,
+                                          N, dk, dv, chunk, io, mask_mode, fl, ctypes.byref(rule),
+                                          _ptr(out), _ptr(S_final), _ptr(workspace),
+                                          0 if workspace is None else workspace.numel(),
+                                          _stream(stream))
+    del keep
+    _check(rc, "linattn_chunked_forward_rule")
+    return out, S_final, M_final
 
 
 def linattn_chunked_forward_noalloc(q, k, v, eta, chunk: int, mask_mode: int,

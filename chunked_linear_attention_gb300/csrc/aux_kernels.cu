@@ -244,48 +244,139 @@ cudaError_t launch_scale_rows(const void* v, const float* eta, void* vt, long lo
 // the chunks visible to chunk c (earlier chunks for apply-then-update, also
 // chunk c otherwise; only flagged chunks in strided mode).  One thread per
 // state element and (batch, head), scanning the chunks in order.
+__device__ __forceinline__ bool chunk_flag(const UpdateFlags& f, int c) {
+  return f.all || ((f.bits[c >> 5] >> (c & 31)) & 1u);
+}
+
 template <typename T>
 __global__ void linattn_prefix_kernel(const float* __restrict__ partials,
                                       const float* __restrict__ S0, T* __restrict__ s_read,
                                       float* __restrict__ s_final, int BH, int nc, int splits,
-                                      int dvdk, int apply_first, UpdateFlags flags) {
+                                      int dvdk, int apply_first, UpdateFlags flags, LinRule rule,
+                                      int compact, int n_upd) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long long)BH * dvdk) return;
   const long long bh = i / dvdk;
   const int e = (int)(i - bh * dvdk);
   float s = S0 ? S0[i] : 0.f;
+  float m = rule.M0 ? rule.M0[i] : 0.f;
+  int u = 0;
   for (int c = 0; c < nc; ++c) {
-    const bool upd = flags.all || ((flags.bits[c >> 5] >> (c & 31)) & 1u);
-    float add = 0.f;
+    const bool upd = chunk_flag(flags, c);
+    float inc = 0.f;
     if (upd) {
-      const float* p = partials + ((bh * nc + c) * (long long)splits) * dvdk + e;
+      float add = 0.f;
+      const float* p = compact ? partials + (bh * n_upd + u) * (long long)dvdk + e
+                               : partials + ((bh * nc + c) * (long long)splits) * dvdk + e;
       for (int sp = 0; sp < splits; ++sp) add += p[(long long)sp * dvdk];
+      const float lr = rule.lr ? rule.lr[bh * nc + c] : 1.f;
+      if (rule.mom) {
+        m = (rule.alpha ? rule.alpha[bh * nc + c] : 0.f) * m + add;
+        inc = lr * m;
+      } else {
+        inc = lr * add;
+      }
+      ++u;
     }
     if (apply_first) {
       s_read[(bh * nc + c) * (long long)dvdk + e] = from_f<T>(s);
-      s += add;
+      s += inc;
     } else {
-      s += add;
+      s += inc;
       s_read[(bh * nc + c) * (long long)dvdk + e] = from_f<T>(s);
     }
   }
   if (s_final) s_final[i] = s;
+  if (rule.M_final) rule.M_final[i] = m;
 }
 
 cudaError_t launch_linattn_prefix(const float* partials, const float* S0, void* s_read,
                                   float* s_final, int BH, int nc, int splits, int dvdk,
-                                  int apply_first, const UpdateFlags& flags, bool bf16,
-                                  cudaStream_t stream) {
+                                  int apply_first, const UpdateFlags& flags, const LinRule& rule,
+                                  int compact, int n_upd, bool bf16, cudaStream_t stream) {
   const long long n = (long long)BH * dvdk;
   const int blocks = (int)((n + 255) / 256);
   if (bf16)
     linattn_prefix_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
         partials, S0, static_cast<__nv_bfloat16*>(s_read), s_final, BH, nc, splits, dvdk,
-        apply_first, flags);
+        apply_first, flags, rule, compact, n_upd);
   else
     linattn_prefix_kernel<float><<<blocks, 256, 0, stream>>>(
         partials, S0, static_cast<float*>(s_read), s_final, BH, nc, splits, dvdk, apply_first,
+        flags, rule, compact, n_upd);
+  return cudaGetLastError();
+}
+
+int linattn_momentum_slots(int dvdk) { return (dvdk + 255) / 256; }
+
+// One block = 256 consecutive elements of one batch-head's state; the block's
+// squared-norm share of every update is reduced in a fixed order (warp
+// shuffles, then the eight warp sums in order).
+template <typename T>
+__global__ void __launch_bounds__(256)
+    linattn_momentum_kernel(const float* __restrict__ partials, int splits, LinRule rule,
+                            T* __restrict__ x, float* __restrict__ norm_part, int BH, int nc,
+                            int n_upd, int dvdk, UpdateFlags flags) {
+  __shared__ float wsum[8];
+  const int nslot = (dvdk + 255) / 256;
+  const int bh = blockIdx.x / nslot, blk = blockIdx.x % nslot;
+  const int e = blk * 256 + threadIdx.x;
+  const bool own = e < dvdk;
+  const long long i = (long long)bh * dvdk + e;
+  float m = (own && rule.M0) ? rule.M0[i] : 0.f;
+  int u = 0;
+  for (int c = 0; c < nc; ++c) {
+    if (!chunk_flag(flags, c)) continue;
+    float add = 0.f;
+    if (own) {
+      const float* p = partials + (((long long)bh * nc + c) * splits) * dvdk + e;
+      for (int sp = 0; sp < splits; ++sp) add += p[(long long)sp * dvdk];
+      m = (rule.alpha ? rule.alpha[(long long)bh * nc + c] : 0.f) * m + add;
+      x[((long long)bh * n_upd + u) * dvdk + e] = from_f<T>(m);
+    }
+    float sq = own ? m * m : 0.f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+    if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = sq;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float t = 0.f;
+      for (int w = 0; w < 8; ++w) t += wsum[w];
+      norm_part[((long long)bh * n_upd + u) * nslot + blk] = t;
+    }
+    __syncthreads();
+    ++u;
+  }
+  if (own && rule.M_final) rule.M_final[i] = m;
+}
+
+cudaError_t launch_linattn_momentum(const float* partials, int splits, const LinRule& rule,
+                                    void* x, float* norm_part, int BH, int nc, int n_upd,
+                                    int dvdk, const UpdateFlags& flags, bool bf16,
+                                    cudaStream_t stream) {
+  const int blocks = BH * linattn_momentum_slots(dvdk);
+  if (bf16)
+    linattn_momentum_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
+        partials, splits, rule, static_cast<__nv_bfloat16*>(x), norm_part, BH, nc, n_upd, dvdk,
         flags);
+  else
+    linattn_momentum_kernel<float><<<blocks, 256, 0, stream>>>(
+        partials, splits, rule, static_cast<float*>(x), norm_part, BH, nc, n_upd, dvdk, flags);
+  return cudaGetLastError();
+}
+
+__global__ void normsq_sum_kernel(const float* __restrict__ part, int nslot,
+                                  float* __restrict__ out, int Z) {
+  const int w = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  if (w >= Z) return;
+  const float s = sum_partials_warp(part + (long long)w * nslot, nslot);
+  if ((threadIdx.x & 31) == 0) out[w] = s;
+}
+
+cudaError_t launch_normsq_sum(const float* part, int nslot, float* out, int Z,
+                              cudaStream_t stream) {
+  if (Z <= 0) return cudaSuccess;
+  normsq_sum_kernel<<<(Z * 32 + 255) / 256, 256, 0, stream>>>(part, nslot, out, Z);
   return cudaGetLastError();
 }
 

@@ -293,6 +293,78 @@ int linattn_chunked_forward(const void* q, const void* k, const void* v, const f
   return ttt::linattn_forward(a, D, st, g_wait_limit_ns);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Validates a linear-attention rule and fills the dims/args fields it sets.
+int apply_lin_rule(const linattn_rule* rule, ttt::LinDims* D, ttt::LinArgs* a) {
+  if (!rule) return TTT_OK;
+  if (rule->muon_steps < 0 || rule->muon_steps > 64) return TTT_ERR_ARG;
+  if (rule->muon_steps > 0 &&
+      (!std::isfinite(rule->ns_a) || !std::isfinite(rule->ns_b) || !std::isfinite(rule->ns_c)))
+    return TTT_ERR_ARG;
+  if ((rule->alpha && (reinterpret_cast<uintptr_t>(rule->alpha) & 3)) ||
+      (rule->lr && (reinterpret_cast<uintptr_t>(rule->lr) & 3)) ||
+      (rule->M0 && !aligned16(rule->M0)) || (rule->M_final && !aligned16(rule->M_final)))
+    return TTT_ERR_ALIGN;
+  D->mom = (rule->alpha || rule->M0 || rule->M_final) ? 1 : 0;
+  D->muon_steps = rule->muon_steps;
+  D->ns[0] = rule->ns_a;
+  D->ns[1] = rule->ns_b;
+  D->ns[2] = rule->ns_c;
+  if (a) {
+    a->alpha = rule->alpha;
+    a->lr = rule->lr;
+    a->M0 = rule->M0;
+    a->M_final = rule->M_final;
+  }
+  return TTT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t linattn_rule_workspace_size(int B, int H, int N, int d_k, int d_v, int chunk, int io_dtype,
+                                   int mask_mode, const linattn_rule* rule) {
+  ttt::LinDims D;
+  if (check_lin(B, H, N, d_k, d_v, chunk, io_dtype, mask_mode, &D) != TTT_OK) return 0;
+  if (apply_lin_rule(rule, &D, nullptr) != TTT_OK) return 0;
+  return ttt::linattn_workspace_bytes(D);
+}
+
+int linattn_chunked_forward_rule(const void* q, const void* k, const void* v, const float* eta,
+                                 const float* S0, int B, int H, int N, int d_k, int d_v,
+                                 int chunk, int io_dtype, int mask_mode,
+                                 const unsigned char* update_chunks, const linattn_rule* rule,
+                                 void* out, float* S_final, void* workspace,
+                                 size_t workspace_bytes, ttt_stream_t stream) {
+  if (!q || !k || !v || !eta || !out) return TTT_ERR_NULL;
+  ttt::LinDims D;
+  int rc = check_lin(B, H, N, d_k, d_v, chunk, io_dtype, mask_mode, &D);
+  if (rc != TTT_OK) return rc;
+  if (mask_mode == TTT_STRIDED && !update_chunks) return TTT_ERR_NULL;
+  const void* ptrs[] = {q, k, v, eta, S0, out, S_final};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return TTT_ERR_ALIGN;
+  ttt::LinArgs a;
+  rc = apply_lin_rule(rule, &D, &a);
+  if (rc != TTT_OK) return rc;
+  const size_t need = ttt::linattn_workspace_bytes(D);
+  if (!workspace || workspace_bytes < need) return TTT_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return TTT_ERR_ALIGN;
+  int* st = status_ptr();
+  if (!st) return TTT_ERR_CUDA;
+  a.q = q; a.k = k; a.v = v; a.eta = eta; a.S0 = S0;
+  a.update_chunks = update_chunks;
+  a.out = out;
+  a.S_final = S_final;
+  a.workspace = workspace;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  return ttt::linattn_forward(a, D, st, g_wait_limit_ns);
+}
+
 int ttt_device_status(ttt_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return TTT_ERR_CUDA;

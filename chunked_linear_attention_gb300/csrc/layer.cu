@@ -36,6 +36,7 @@
 #include "exec.h"
 #include "ns_cluster.h"
 #include "ns_half.h"
+#include "ns_products.h"
 #include "prof.h"
 
 namespace ttt {
@@ -440,99 +441,26 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
       if (h0 != 0 || nh != BH) return -4;   // per-product path runs over all sequences
       TTT_CK(launch_normsq_reduce(w.normsq_part, w.nslot, w.normsq, BH, 0, BH, st));
       const int sdim = std::min(d, m);
+      const long long ss = (long long)sdim * sdim;
       // groups of equally shaped slots: {0,1,2} if square, else {0,1} and {2}
-      int groups[2][2];  // first slot, count
-      int ng = 0;
-      if (d == m) {
-        groups[0][0] = 0; groups[0][1] = 3; ng = 1;
-      } else {
-        groups[0][0] = 0; groups[0][1] = 2; groups[1][0] = 2; groups[1][1] = 1; ng = 2;
+      NsGroup groups[2];
+      const int gfirst[2] = {0, 2}, gcount[2] = {d == m ? 3 : 2, 1};
+      const int ng = d == m ? 1 : 2;
+      for (int g = 0; g < ng; ++g) {
+        const int s0 = gfirst[g];
+        NsGroup& q = groups[g];
+        q.X[0] = offs(w.X[0], (long long)s0 * BH * dm);
+        q.X[1] = offs(w.X[1], (long long)s0 * BH * dm);
+        q.G = offs(w.G, (long long)s0 * BH * ss);
+        q.Bm = offs(w.Bm, (long long)s0 * BH * ss);
+        q.U = w.U + (long long)s0 * BH * dm;
+        q.normsq = w.normsq + (long long)s0 * BH;
+        q.Z = gcount[g] * BH;
+        q.R = rows_of[s0];
+        q.C = cols_of[s0];
       }
-      const int wb16 = tc ? 1 : 0;
-      for (int t = 0; t < D.muon_steps; ++t) {
-        const int in = t & 1;
-        const bool last = t == D.muon_steps - 1;
-        // GRAM: G = X X^T (or X^T X for tall slots), scaled on the first step
-        for (int g = 0; g < ng; ++g) {
-          const int s0 = groups[g][0], cnt = groups[g][1];
-          const int R = rows_of[s0], C = cols_of[s0];
-          const int Z = cnt * BH;
-          TensorRef TX{offs(w.X[in], (long long)s0 * BH * dm), wb16, (long long)Z * R, C};
-          const int bn = LB.choose_bn(sdim, 1);
-          Problem p = prob0(sdim, sdim, std::max(R, C), Z, 1, bn);
-          if (R <= C) {
-            p.a[0] = LB.op(TX, 0, 0, R, BM);
-            p.b[0] = LB.op(TX, 0, 0, R, bn);
-          } else {
-            p.a[0] = LB.op(TX, 1, 0, R, 64);
-            p.b[0] = LB.op(TX, 1, 0, R, 64);
-          }
-          p.epi.kind = EPI_NS_GRAM;
-          p.epi.out[0] = offs(w.G, (long long)s0 * BH * sdim * sdim);
-          p.epi.out_ld = sdim;
-          p.epi.out_z = (long long)sdim * sdim;
-          p.epi.first = t == 0;
-          p.epi.normsq = w.normsq + (long long)s0 * BH;
-          p.epi.eps = 1e-7f;
-          LB.add(p);
-        }
-        if (!LB.ok()) return -4;
-        TTT_CK(LB.launch(st, PT_NS_GRAM));
-        // POLY: Bm = b G + c G G (G symmetric)
-        for (int g = 0; g < ng; ++g) {
-          const int s0 = groups[g][0], cnt = groups[g][1];
-          const int Z = cnt * BH;
-          TensorRef TG{offs(w.G, (long long)s0 * BH * sdim * sdim), wb16, (long long)Z * sdim,
-                       sdim};
-          const int bn = LB.choose_bn(sdim, 1);
-          Problem p = prob0(sdim, sdim, sdim, Z, 1, bn);
-          p.a[0] = LB.op(TG, 0, 0, sdim, BM);
-          p.b[0] = LB.op(TG, 0, 0, sdim, bn);
-          p.epi.kind = EPI_NS_POLY;
-          p.epi.in0 = TG.ptr;
-          p.epi.out[0] = offs(w.Bm, (long long)s0 * BH * sdim * sdim);
-          p.epi.out_ld = sdim;
-          p.epi.out_z = (long long)sdim * sdim;
-          p.epi.b = D.ns[1];
-          p.epi.c = D.ns[2];
-          LB.add(p);
-        }
-        if (!LB.ok()) return -4;
-        TTT_CK(LB.launch(st, PT_NS_POLY));
-        // STEP: X' = s (a X + Bm X) (or X Bm for tall slots, in stored orientation)
-        for (int g = 0; g < ng; ++g) {
-          const int s0 = groups[g][0], cnt = groups[g][1];
-          const int R = rows_of[s0], C = cols_of[s0];
-          const int Z = cnt * BH;
-          TensorRef TX{offs(w.X[in], (long long)s0 * BH * dm), wb16, (long long)Z * R, C};
-          TensorRef TB{offs(w.Bm, (long long)s0 * BH * sdim * sdim), wb16, (long long)Z * sdim,
-                       sdim};
-          const int bn = LB.choose_bn(C, 1);
-          Problem p = prob0(R, C, sdim, Z, 1, bn);
-          if (R <= C) {
-            p.a[0] = LB.op(TB, 0, 0, sdim, BM);
-            p.b[0] = LB.op(TX, 1, 0, R, 64);
-          } else {
-            p.a[0] = LB.op(TX, 0, 0, R, BM);
-            p.b[0] = LB.op(TB, 0, 0, sdim, bn);
-          }
-          p.epi.kind = EPI_NS_STEP;
-          p.epi.in0 = TX.ptr;
-          if (last)
-            p.epi.out[1] = w.U + (long long)s0 * BH * dm;
-          else
-            p.epi.out[0] = offs(w.X[in ^ 1], (long long)s0 * BH * dm);
-          p.epi.out_ld = C;
-          p.epi.out_z = dm;
-          p.epi.a = D.ns[0];
-          p.epi.first = t == 0;
-          p.epi.normsq = w.normsq + (long long)s0 * BH;
-          p.epi.eps = 1e-7f;
-          LB.add(p);
-        }
-        if (!LB.ok()) return -4;
-        TTT_CK(LB.launch(st, PT_NS_STEP));
-      }
+      const int rc = enqueue_ns_products(LB, groups, ng, D.muon_steps, D.ns, st);
+      if (rc != 0) return rc;
     }
 
     // ---------------- NORM

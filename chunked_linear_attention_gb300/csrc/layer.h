@@ -57,6 +57,9 @@ struct LinDims {
   int B, H, N, dk, dv, chunk;
   bool bf16;
   int mode;
+  int mom = 0;              // a momentum accumulator is carried (alpha, M0 or M_final given)
+  int muon_steps = 0;       // Newton-Schulz steps of Muon(M) per update (0: none)
+  float ns[3] = {0.f, 0.f, 0.f};
 };
 
 struct LinArgs {
@@ -70,6 +73,10 @@ struct LinArgs {
   float* S_final;
   void* workspace;
   cudaStream_t stream;
+  const float* alpha = nullptr;   // [B*H][nc] momentum factor per chunk, or NULL (0)
+  const float* lr = nullptr;      // [B*H][nc] learning rate per chunk, or NULL (1)
+  const float* M0 = nullptr;      // [B*H][dv*dk] initial momentum, or NULL (zeros)
+  float* M_final = nullptr;       // [B*H][dv*dk] final momentum, or NULL
 };
 
 size_t linattn_workspace_bytes(const LinDims& D);

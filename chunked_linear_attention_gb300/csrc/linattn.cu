@@ -14,9 +14,11 @@
 #include <cstring>
 
 #include "builder.h"
+#include "launch.h"
 #include "layer.h"
 #include "linattn_fused.h"
 #include "linattn_kernels.h"
+#include "ns_products.h"
 #include "prof.h"
 
 namespace ttt {
@@ -48,6 +50,14 @@ struct LinWs {
   float* partials;
   void* Sread;
   int splits;
+  // Muon of the momentum (one matrix per update of every sequence)
+  void* X[2];
+  void* G;
+  void* Bm;
+  float* U;
+  float* normsq;
+  float* norm_part;
+  int nslot;
 };
 
 size_t lin_layout(const LinDims& D, LinWs* w, char* base) {
@@ -69,6 +79,20 @@ size_t lin_layout(const LinDims& D, LinWs* w, char* base) {
   o.Vt = take(BH * D.N * D.dv * es);
   o.partials = reinterpret_cast<float*>(take(BH * nc * splits * D.dv * D.dk * 4));
   o.Sread = take(BH * nc * D.dv * D.dk * es);
+  o.nslot = linattn_momentum_slots(D.dv * D.dk);
+  if (D.muon_steps > 0) {   // sized for every chunk updating
+    const size_t Z = BH * nc, E = (size_t)D.dv * D.dk, sm = std::min(D.dv, D.dk);
+    o.X[0] = take(Z * E * es);
+    o.X[1] = take(Z * E * es);
+    o.G = take(Z * sm * sm * es);
+    o.Bm = take(Z * sm * sm * es);
+    o.U = reinterpret_cast<float*>(take(Z * E * 4));
+    o.normsq = reinterpret_cast<float*>(take(Z * 4));
+    o.norm_part = reinterpret_cast<float*>(take(Z * o.nslot * 4));
+  } else {
+    o.X[0] = o.X[1] = o.G = o.Bm = nullptr;
+    o.U = o.normsq = o.norm_part = nullptr;
+  }
   return off;
 }
 
@@ -92,7 +116,7 @@ Problem prob0(int M, int N, int K, int Z, int nacc, int bn) {
 // cooperative launch).
 size_t linattn_workspace_bytes(const LinDims& D) {
   size_t n = lin_layout(D, nullptr, nullptr);
-  if (linattn_fused_applicable(D))
+  if (D.muon_steps == 0 && linattn_fused_applicable(D))
     n = std::max(n, linattn_fused_scratch(D, linattn_fused_plan(D)));
   return n;
 }
@@ -107,11 +131,24 @@ int linattn_forward(const LinArgs& a, const LinDims& D, int* status, unsigned lo
   UpdateFlags flags;
   std::memset(&flags, 0, sizeof(flags));
   flags.all = D.mode != 3;
-  if (D.mode == 3)
+  int n_upd = nc;
+  if (D.mode == 3) {
+    n_upd = 0;
     for (int c = 0; c < nc; ++c)
-      if (a.update_chunks[c]) flags.bits[c >> 5] |= 1u << (c & 31);
+      if (a.update_chunks[c]) {
+        flags.bits[c >> 5] |= 1u << (c & 31);
+        ++n_upd;
+      }
+  }
+  LinRule rule;
+  rule.alpha = a.alpha;
+  rule.lr = a.lr;
+  rule.M0 = a.M0;
+  rule.M_final = a.M_final;
+  rule.mom = D.mom;
+  const bool muon = D.muon_steps > 0;
 
-  if (linattn_fused_applicable(D)) {
+  if (!muon && linattn_fused_applicable(D)) {
     MapCache fcache;
     LinFusedArgs fa;
     fa.D = &D;
@@ -121,6 +158,7 @@ int linattn_forward(const LinArgs& a, const LinDims& D, int* status, unsigned lo
     fa.eta = a.eta;
     fa.S0 = a.S0;
     fa.flags = &flags;
+    fa.rule = rule;
     fa.out = a.out;
     fa.S_final = a.S_final;
     fa.scratch = a.workspace;
@@ -162,11 +200,51 @@ int linattn_forward(const LinArgs& a, const LinDims& D, int* status, unsigned lo
     if (!LB.ok()) return -4;
     if (LB.launch(st, PT_LIN_PARTIAL) != cudaSuccess) return -6;
   }
-  {
+  const int dvdk = dv * dk;
+  if (!muon) {
     ProfScope ps(PT_LIN_PREFIX, st, 0.0,
-                 (double)BH * nc * dv * dk * (4.0 * splits + (tc ? 2 : 4)));
-    if (launch_linattn_prefix(w.partials, a.S0, w.Sread, a.S_final, BH, nc, splits, dv * dk,
-                              D.mode == 0, flags, tc, st) != cudaSuccess)
+                 (double)BH * nc * dvdk * (4.0 * splits + (tc ? 2 : 4)));
+    if (launch_linattn_prefix(w.partials, a.S0, w.Sread, a.S_final, BH, nc, splits, dvdk,
+                              D.mode == 0, flags, rule, 0, n_upd, tc, st) != cudaSuccess)
+      return -6;
+  } else if (n_upd == 0) {   // nothing updates: every chunk reads S0
+    LinRule none = {};
+    if (launch_linattn_prefix(w.partials, a.S0, w.Sread, a.S_final, BH, nc, splits, dvdk,
+                              D.mode == 0, flags, none, 0, 0, tc, st) != cudaSuccess)
+      return -6;
+    if (a.M_final && launch_copy_f32(a.M_final, a.M0, (long long)BH * dvdk, st) != cudaSuccess)
+      return -6;
+  } else {
+    // Muon of every update's momentum ("Test-Time Training with KV Binding Is
+    // Secretly Linear Attention", App. E.3): the momenta M_u of all updates
+    // at once, their squared norms, the Newton-Schulz products over all of
+    // them, then the state prefix of lr_c Muon(M_u)
+    {
+      ProfScope ps(PT_LIN_PREFIX, st, 0.0, (double)BH * nc * dvdk * (4.0 * splits + (tc ? 2 : 4)));
+      if (launch_linattn_momentum(w.partials, splits, rule, w.X[0], w.norm_part, BH, nc, n_upd,
+                                  dvdk, flags, tc, st) != cudaSuccess)
+        return -6;
+    }
+    const int Z = BH * n_upd;
+    if (launch_normsq_sum(w.norm_part, w.nslot, w.normsq, Z, st) != cudaSuccess) return -6;
+    NsGroup g;
+    g.X[0] = w.X[0];
+    g.X[1] = w.X[1];
+    g.G = w.G;
+    g.Bm = w.Bm;
+    g.U = w.U;
+    g.normsq = w.normsq;
+    g.Z = Z;
+    g.R = dv;
+    g.C = dk;
+    LB.reset();
+    const int rc = enqueue_ns_products(LB, &g, 1, D.muon_steps, D.ns, st);
+    if (rc != 0) return rc;
+    LinRule upd_rule = {};
+    upd_rule.lr = a.lr;
+    ProfScope ps(PT_LIN_PREFIX, st, 0.0, (double)BH * nc * dvdk * (4.0 + (tc ? 2 : 4)));
+    if (launch_linattn_prefix(w.U, a.S0, w.Sread, a.S_final, BH, nc, 1, dvdk, D.mode == 0, flags,
+                              upd_rule, 1, n_upd, tc, st) != cudaSuccess)
       return -6;
   }
   {  // outputs

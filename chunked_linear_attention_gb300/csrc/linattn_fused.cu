@@ -65,6 +65,7 @@ struct LinFusedLaunch {
   int nA, nP, nB, nstages;
   uint32_t stage_bytes;
   UpdateFlags flags;
+  LinRule rule;               // momentum and per-chunk learning rates of the state update
   int* status;
   unsigned long long wait_limit_ns;
   int withhold_bh;            // test hook: this batch-head's A items never release (-1: none)
@@ -155,18 +156,27 @@ __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* r, float4 v) {
   *reinterpret_cast<uint2*>(r) = u;
 }
 
+__device__ __forceinline__ void fma4(float4& y, float a, const float4& x) {
+  y.x = fmaf(a, x.x, y.x); y.y = fmaf(a, x.y, y.y); y.z = fmaf(a, x.z, y.z); y.w = fmaf(a, x.w, y.w);
+}
+
+// Per updating chunk c: M <- alpha_c M + G_c, S <- S + lr_c M (rule.mom), or
+// S <- S + lr_c G_c; chunks that do not update leave both unchanged.
 __device__ __forceinline__ void prefix_item(const LinFusedLaunch& L, int bh, int e0, int e1,
                                             int tid) {
   const long long E = (long long)L.dv * L.dk;
   const int npairs = L.nc * L.splits;
+  const LinRule& R = L.rule;
   for (int eb = e0; eb < e1; eb += 4 * 128 * kPG) {
-    float4 s[kPG], add[kPG];
+    float4 s[kPG], add[kPG], m[kPG];
     bool own[kPG];
 #pragma unroll
     for (int g = 0; g < kPG; ++g) {
       const int e = eb + 4 * tid + 512 * g;
       own[g] = e < e1;
       s[g] = (own[g] && L.S0) ? *reinterpret_cast<const float4*>(L.S0 + bh * E + e)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+      m[g] = (own[g] && R.M0) ? *reinterpret_cast<const float4*>(R.M0 + bh * E + e)
                               : make_float4(0.f, 0.f, 0.f, 0.f);
       add[g] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
@@ -195,24 +205,39 @@ __device__ __forceinline__ void prefix_item(const LinFusedLaunch& L, int bh, int
         if ((pr + 1) % L.splits != 0) continue;
         // chunk pr / splits complete: the state it reads, then the running state
         const int c = pr / L.splits;
+        const bool upd = chunk_updates(L, c);
+        const float lr = (upd && R.lr) ? R.lr[(long long)bh * L.nc + c] : 1.f;
+        const float al = (upd && R.mom && R.alpha) ? R.alpha[(long long)bh * L.nc + c] : 0.f;
 #pragma unroll
         for (int g = 0; g < kPG; ++g) {
           if (!own[g]) continue;
+          float4 inc = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (upd) {
+            if (R.mom) {
+              float4 mm = add[g];
+              fma4(mm, al, m[g]);
+              m[g] = mm;
+              fma4(inc, lr, mm);
+            } else {
+              fma4(inc, lr, add[g]);
+            }
+          }
           float4 rd = s[g];
           if (!L.apply_first) {
-            rd.x += add[g].x; rd.y += add[g].y; rd.z += add[g].z; rd.w += add[g].w;
+            rd.x += inc.x; rd.y += inc.y; rd.z += inc.z; rd.w += inc.w;
           }
           store_bf16x4(L.s_read + (long long)(bh * L.nc + c) * E + eb + 4 * tid + 512 * g, rd);
-          s[g].x += add[g].x; s[g].y += add[g].y; s[g].z += add[g].z; s[g].w += add[g].w;
+          s[g].x += inc.x; s[g].y += inc.y; s[g].z += inc.z; s[g].w += inc.w;
           add[g] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
     }
-    if (L.s_final) {
 #pragma unroll
-      for (int g = 0; g < kPG; ++g)
-        if (own[g])
-          *reinterpret_cast<float4*>(L.s_final + bh * E + eb + 4 * tid + 512 * g) = s[g];
+    for (int g = 0; g < kPG; ++g) {
+      if (!own[g]) continue;
+      const long long o = bh * E + eb + 4 * tid + 512 * g;
+      if (L.s_final) *reinterpret_cast<float4*>(L.s_final + o) = s[g];
+      if (R.M_final) *reinterpret_cast<float4*>(R.M_final + o) = m[g];
     }
   }
 }
@@ -634,6 +659,7 @@ int launch_linattn_fused(MapCache& cache, const LinFusedArgs& a, int* status,
   L.rb = p.rb;
   L.apply_first = D.mode == 0;
   L.flags = *a.flags;
+  L.rule = a.rule;
   int n_upd = 0;
   for (int c = 0; c < nc; ++c)
     if (L.flags.all || ((L.flags.bits[c >> 5] >> (c & 31)) & 1u)) ++n_upd;

@@ -23,6 +23,7 @@ struct LinFusedArgs {
   const float* eta;
   const float* S0;              // or NULL
   const UpdateFlags* flags;
+  LinRule rule;                 // momentum / per-chunk learning rates (no Muon here)
   void* out;
   float* S_final;               // or NULL
   void* scratch;                // linattn_fused_scratch() bytes, 256-byte aligned

@@ -199,6 +199,54 @@ int linattn_chunked_forward(const void* q, const void* k, const void* v, const f
                             void* out, float* S_final,
                             void* workspace, size_t workspace_bytes, ttt_stream_t stream);
 
+/* Momentum, per-chunk learning rate and Muon of the linear-attention state
+ * update: the reducible TTT variants ("Test-Time Training with KV Binding Is
+ * Secretly Linear Attention", Thm 5.3 / App. D for gradient descent with a
+ * per-step momentum factor, App. H for its chunk form with per-chunk
+ * learning rates, App. E.3 for Muon applied to the momentum accumulator;
+ * sec. 6.1 Variants 3-6 are the single-linear-layer cases).  Per (batch,
+ * head) and updating chunk t, with G_t = sum over the chunk's tokens of
+ * eta_i v_i k_i^T:
+ *     M_t = alpha_t M_{t-1} + G_t          (M_{-1} = M0)
+ *     U_t = Muon(M_t) (muon_steps > 0) or M_t
+ *     S   <- S + lr_t U_t
+ * Chunks a strided mask does not update leave M and S unchanged.
+ *   alpha     device fp32 [B, H, N/chunk]: momentum factor of each chunk, or
+ *             NULL (0: no momentum; M_t = G_t).
+ *   lr        device fp32 [B, H, N/chunk]: learning rate of each chunk, or
+ *             NULL (1).
+ *   M0        device fp32 [B, H, d_v, d_k] initial momentum, or NULL (zeros).
+ *   M_final   device fp32 [B, H, d_v, d_k]: the momentum after the last chunk,
+ *             or NULL (not written).  May alias M0.
+ *   muon_steps, ns_a/ns_b/ns_c: as in ttt_update_rule (Muon scales M_t to
+ *             unit Frobenius norm, eps 1e-7, and orients the smaller side). */
+typedef struct {
+  const float* alpha;
+  const float* lr;
+  const float* M0;
+  float* M_final;
+  int muon_steps;
+  float ns_a, ns_b, ns_c;
+} linattn_rule;
+
+/* Bytes of device workspace linattn_chunked_forward_rule needs (0 if the
+ * arguments are invalid).  rule may be NULL (plain linear attention). */
+size_t linattn_rule_workspace_size(int B, int H, int N, int d_k, int d_v, int chunk,
+                                   int io_dtype, int mask_mode, const linattn_rule* rule);
+
+/* linattn_chunked_forward with the update rule above (HOST pointer `rule`;
+ * NULL, or alpha = lr = M0 = M_final = NULL with muon_steps = 0, computes
+ * exactly what linattn_chunked_forward computes).  Same tensors, shapes,
+ * support and status codes; alpha and lr must be 4-byte aligned, M0 and
+ * M_final 16-byte aligned.  With Muon the bf16 path rounds each M_t to bf16
+ * for the Newton-Schulz products (fp32 accumulation), like the layer. */
+int linattn_chunked_forward_rule(const void* q, const void* k, const void* v, const float* eta,
+                                 const float* S0, int B, int H, int N, int d_k, int d_v,
+                                 int chunk, int io_dtype, int mask_mode,
+                                 const unsigned char* update_chunks, const linattn_rule* rule,
+                                 void* out, float* S_final, void* workspace,
+                                 size_t workspace_bytes, ttt_stream_t stream);
+
 /* linattn_chunked_forward for callers that cannot allocate device memory.
  * The pages have no counterpart for this call; it exists because some
  * callers cannot call cudaMalloc (a host framework that owns the GPU memory
