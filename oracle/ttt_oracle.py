@@ -190,15 +190,19 @@ def _update_flags(n_chunks, mode, update_chunks):
 
 
 def chunk_scan(Q, K, V, eta, Ws, chunk, mode, update_chunks, apply_fn, grad_fn,
-               dynamic, l2norm, muon_steps, beta, coef, Ms, n_chunks=None):
+               dynamic, l2norm, muon_steps, beta, coef, Ms, n_chunks=None, inner_steps=1):
     """Sequential chunk recurrence for one (batch, head).
 
     Q, K, V: [N, d]; eta: [N]; Ws: list of fast-weight matrices; Ms: list of
     momentum matrices (same shapes).  ``dynamic[i]`` says whether Ws[i] is
     updated.  Apply-then-update uses the state from before the chunk (eq 10);
     the other masks update first, then apply.  Strided mode only updates on
-    flagged chunks.  ``n_chunks`` limits the scan to a prefix of the sequence
-    (outputs past the prefix stay zero).
+    flagged chunks.  ``inner_steps`` updates are taken on each updating
+    chunk, each from the gradient at the current weights ("Test-Time
+    Training with KV Binding Is Secretly Linear Attention", sec. 4.1: more
+    inner-loop steps at test time); the apply reads the weights before the
+    first or after the last of them.  ``n_chunks`` limits the scan to a
+    prefix of the sequence (outputs past the prefix stay zero).
     Returns (O, Ws, Ms).
     """
     N = Q.shape[0]
@@ -217,11 +221,12 @@ def chunk_scan(Q, K, V, eta, Ws, chunk, mode, update_chunks, apply_fn, grad_fn,
         if mode == APPLY_THEN_UPDATE:
             O[sl] = apply_fn(Ws, Q[sl])
         if flags[c]:
-            gs = grad_fn(Ws, K[sl], V[sl], eta[sl])
-            for i, g in enumerate(gs):
-                if dynamic[i]:
-                    Ws[i], Ms[i] = update_one_matrix(Ws[i], g, Ms[i], l2norm,
-                                                     muon_steps, beta, coef)
+            for _ in range(max(1, inner_steps)):
+                gs = grad_fn(Ws, K[sl], V[sl], eta[sl])
+                for i, g in enumerate(gs):
+                    if dynamic[i]:
+                        Ws[i], Ms[i] = update_one_matrix(Ws[i], g, Ms[i], l2norm,
+                                                         muon_steps, beta, coef)
         if mode != APPLY_THEN_UPDATE:
             O[sl] = apply_fn(Ws, Q[sl])
     return O, Ws, Ms
@@ -240,12 +245,13 @@ def _per_batch(W, B):
 def ttt_layer_forward(q, k, v, eta, W1, W2, W3, chunk, mode, update_chunks=None,
                       l2norm=True, muon_steps=0, momentum_beta=0.0,
                       ns_coef=MUON_COEF, momentum=None, last_layer_only=False,
-                      n_chunks=None):
+                      n_chunks=None, inner_steps=1):
     """LaCT TTT layer forward over [B, H, N, d] inputs.
 
     W1, W3: [H, m, d] or [B, H, m, d]; W2: [H, d, m] or [B, H, d, m].
     momentum: optional (M1, M2, M3) with shapes [B, H, ...] carried in; zero
     otherwise.  ``last_layer_only`` keeps W1, W3 static (only W2 updates).
+    ``inner_steps``: update steps per updating chunk (see chunk_scan).
     Returns (out [B,H,N,d], W1f, W2f, W3f, (M1, M2, M3)), all float64.
     """
     q, k, v, eta = _f64(q), _f64(k), _f64(v), _f64(eta)
@@ -272,7 +278,8 @@ def ttt_layer_forward(q, k, v, eta, W1, W2, W3, chunk, mode, update_chunks=None,
                 Ms = [_f64(momentum[0])[b, h], _f64(momentum[1])[b, h], _f64(momentum[2])[b, h]]
             O, Ws, Ms = chunk_scan(q[b, h], k[b, h], v[b, h], eta[b, h], Ws, chunk, mode,
                                    update_chunks, apply_fn, grad_fn, dynamic, l2norm,
-                                   muon_steps, momentum_beta, ns_coef, Ms, n_chunks)
+                                   muon_steps, momentum_beta, ns_coef, Ms, n_chunks,
+                                   inner_steps)
             out[b, h] = O
             W1f[b, h], W2f[b, h], W3f[b, h] = Ws
             M1f[b, h], M2f[b, h], M3f[b, h] = Ms

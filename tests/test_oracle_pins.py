@@ -400,3 +400,50 @@ def test_replace_q_with_k_runs():
     q, k, v, eta, W1, W2, W3 = _layer_args()
     out, *_ = O.ttt_layer_forward(k, k, v, eta, W1, W2, W3, 8, O.APPLY_THEN_UPDATE)
     assert np.all(np.isfinite(out))
+
+
+# ---------------------------------------------------------------------------
+# more inner-loop steps ("Test-Time Training with KV Binding Is Secretly
+# Linear Attention", sec. 4.1): r update steps on a chunk are r single-step
+# updates on r copies of that chunk
+
+def _repeat_chunks(x, chunk, r):
+    """Every chunk of the sequence axis (axis 2) repeated r times in place."""
+    B, H, N = x.shape[:3]
+    n = N // chunk
+    parts = np.split(x, n, axis=2)
+    return np.concatenate([p for p in parts for _ in range(r)], axis=2)
+
+
+@pytest.mark.parametrize("mode,flags", [(O.APPLY_THEN_UPDATE, None), (O.BLOCK_CAUSAL, None),
+                                        (O.STRIDED, (1, 0, 1))])
+@pytest.mark.parametrize("muon", [0, 2])
+def test_inner_steps_are_repeated_chunks(mode, flags, muon):
+    rng = np.random.default_rng(77)
+    B, H, N, d, m, chunk, r = 1, 2, 12, 4, 6, 4, 3
+    q, k, v = (rng.normal(size=(B, H, N, d)) * 0.5 for _ in range(3))
+    eta = rng.uniform(0.05, 0.3, size=(B, H, N))
+    W1, W3 = (rng.normal(size=(H, m, d)) * 0.5 for _ in range(2))
+    W2 = rng.normal(size=(H, d, m)) * 0.5
+    kw = dict(l2norm=True, muon_steps=muon, momentum_beta=0.6)
+    got = O.ttt_layer_forward(q, k, v, eta, W1, W2, W3, chunk, mode, flags, inner_steps=r,
+                              **kw)
+    rep = [_repeat_chunks(x, chunk, r) for x in (q, k, v, eta[..., None])]
+    # copies of a chunk that the strided mask does not update still only apply
+    rflags = None if flags is None else [f for f in flags for _ in range(r)]
+    ref = O.ttt_layer_forward(rep[0], rep[1], rep[2], rep[3][..., 0], W1, W2, W3, chunk, mode,
+                              rflags, **kw)
+    n = N // chunk
+    # the output of chunk c: the first copy's (apply before the update) or
+    # the last copy's (apply after the updates; a chunk without update
+    # applies the same weights in every copy)
+    pick = 0 if mode == O.APPLY_THEN_UPDATE else r - 1
+    want = np.concatenate([ref[0][:, :, (c * r + pick) * chunk:(c * r + pick + 1) * chunk]
+                           for c in range(n)], axis=2)
+    np.testing.assert_allclose(got[0], want, rtol=1e-10, atol=1e-12)
+    for i in (1, 2, 3):
+        np.testing.assert_allclose(got[i], ref[i], rtol=1e-10, atol=1e-12)
+    # one step is the default
+    one = O.ttt_layer_forward(q, k, v, eta, W1, W2, W3, chunk, mode, flags, inner_steps=1, **kw)
+    base = O.ttt_layer_forward(q, k, v, eta, W1, W2, W3, chunk, mode, flags, **kw)
+    np.testing.assert_array_equal(one[0], base[0])
