@@ -438,6 +438,74 @@ def time_linattn(torch, cla, dev, stream, peaks):
             "io_bytes": io_bytes, "l2": "flushed (256 MB write) before each call"}
 
 
+def time_variants(torch, cla, dev, stream, steps=10, warmup=3):
+    """The reduction path of the linear-attention paper (sec. 6.1, Table 2:
+    TTT-layer tokens/s, recurrent and parallel forms) on the LM workload's
+    shapes and inputs: LaCT; Variant 1 (only W2 updates); Variant 2 (no
+    normalisation; recurrent and parallel); Variants 3-5 (a single linear
+    fast weight d x d with Muon; momentum; per-token or constant eta; parallel
+    form); Variant 6 (plain chunked linear attention)."""
+    import workloads
+    wl = workloads.LM_760M
+    B, H, N, d, m, b = wl.B, wl.H, wl.N, wl.d_h, wl.m_h, wl.chunk
+    q, k, v, eta, W1, W2, W3 = [t.to(dev) for t in workloads.layer_inputs(wl)]
+    nc = N // b
+    res = {}
+
+    def timed(name, fn, form):
+        fn()
+        torch.cuda.synchronize()
+        check_status(cla)
+        ms = time_steps(torch, fn, steps, warmup, stream) / steps
+        check_status(cla)
+        res[name] = {"form": form, "ms_per_call": ms, "tokens_per_s": B * N / (ms / 1e3)}
+
+    out = torch.empty_like(q)
+    Wf = (torch.empty((B, H, m, d), device=dev), torch.empty((B, H, d, m), device=dev),
+          torch.empty((B, H, m, d), device=dev))
+    for name, kw, form in (
+            ("lact", dict(), "recurrent"),
+            ("v1", dict(last_layer_only=True), "recurrent"),
+            ("v2_recurrent", dict(last_layer_only=True, l2norm=False,
+                                  form=cla.FORM_RECURRENT), "recurrent"),
+            ("v2_parallel", dict(last_layer_only=True, l2norm=False,
+                                 form=cla.FORM_PARALLEL), "parallel")):
+        rk = dict(l2norm=True, muon_steps=wl.muon_steps, momentum_beta=wl.momentum_beta)
+        rk.update(kw)
+        rule = cla.update_rule(**rk)
+        ws = torch.empty(cla.layer_workspace_size(B, H, N, d, m, b, cla.TTT_BF16, wl.mode, rule),
+                         device=dev, dtype=torch.uint8)
+        timed(name, lambda: cla.ttt_layer_forward(q, k, v, eta, W1, W2, W3, b, wl.mode, rule,
+                                                  out=out, W_final=Wf, workspace=ws), form)
+        del ws
+    # a single linear fast weight S [d, d] (Variants 3-6), S0 ~ N(0, 1/d)
+    S0 = W2.unsqueeze(0).expand(B, H, d, m).contiguous()
+    beta = torch.full((B, H, nc), wl.momentum_beta, device=dev)
+    eta_c = torch.full_like(eta, 1.0 / b)
+    S = torch.empty((B, H, d, m), device=dev)
+    lo = torch.empty_like(q)
+    for name, e_, al, steps_ in (("v3", eta, beta, wl.muon_steps),
+                                 ("v4", eta_c, beta, wl.muon_steps),
+                                 ("v5", eta_c, None, wl.muon_steps),
+                                 ("v6", eta_c, None, 0)):
+        rule = cla.linattn_rule(alpha=al, muon_steps=steps_)
+        ws = torch.empty(cla.library().linattn_rule_workspace_size(
+            B, H, N, d, d, b, cla.TTT_BF16, wl.mode, ctypes_ref(rule)), device=dev,
+            dtype=torch.uint8)
+        timed(name, lambda: cla.linattn_chunked_forward_rule(
+            q, k, v, e_, b, wl.mode, S0=S0, alpha=al, muon_steps=steps_, out=lo, S_final=S,
+            workspace=ws), "parallel")
+        del ws
+    res["note"] = ("LM workload shapes (B2 H4 d=m=384 N32768 chunk 2048, beta 0.9, Muon 5); "
+                   "Variants 3-6 use q, k, v directly with a 384 x 384 state")
+    return res
+
+
+def ctypes_ref(x):
+    import ctypes
+    return ctypes.byref(x)
+
+
 def run_ours(args):
     import torch
     import chunked_linear_attention_gb300 as cla
@@ -552,6 +620,10 @@ def run_ours(args):
             extra[key] = time_extra_workload(torch, cla, ew, dev, stream, peaks,
                                              steps=5 if big else 20, warmup=3)
 
+    variants = None
+    if not args.skip_variants:
+        variants = time_variants(torch, cla, dev, stream)
+
     cpu = None
     if not args.skip_cpu_baseline:
         rate, desc, _ = oracle_sample(wl, budget_s=args.ref_budget)
@@ -592,6 +664,7 @@ def run_ours(args):
         "clocks": clk,
         "linattn": lin,
         "workloads": extra,
+        "variants": variants,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -611,6 +684,8 @@ def main(argv=None):
     ap.add_argument("--skip-linattn", action="store_true")
     ap.add_argument("--skip-workloads", action="store_true",
                     help="time only the headline workload")
+    ap.add_argument("--skip-variants", action="store_true",
+                    help="skip the reduction variants (Table 2 forms) on the LM workload")
     ap.add_argument("--seq-len", type=int, default=None,
                     help="override the workload's sequence length (small profiling cases)")
     args = ap.parse_args(argv)

@@ -46,11 +46,18 @@ class ProfileEntry(ctypes.Structure):
                 ("sm_ms", ctypes.c_double)]
 
 
+FORM_AUTO = 0
+FORM_RECURRENT = 1
+FORM_PARALLEL = 2
+
+
 class UpdateRule(ctypes.Structure):
     """Mirror of ``ttt_update_rule``."""
     _fields_ = [("l2norm", ctypes.c_int), ("muon_steps", ctypes.c_int),
                 ("momentum_beta", ctypes.c_float), ("ns_a", ctypes.c_float),
-                ("ns_b", ctypes.c_float), ("ns_c", ctypes.c_float)]
+                ("ns_b", ctypes.c_float), ("ns_c", ctypes.c_float),
+                ("last_layer_only", ctypes.c_int), ("inner_steps", ctypes.c_int),
+                ("form", ctypes.c_int)]
 
 
 class LinattnRule(ctypes.Structure):
@@ -60,10 +67,12 @@ class LinattnRule(ctypes.Structure):
                 ("ns_a", ctypes.c_float), ("ns_b", ctypes.c_float), ("ns_c", ctypes.c_float)]
 
 
-def update_rule(l2norm=True, muon_steps=0, momentum_beta=0.0, ns_coef=MUON_COEF) -> UpdateRule:
+def update_rule(l2norm=True, muon_steps=0, momentum_beta=0.0, ns_coef=MUON_COEF,
+                last_layer_only=False, inner_steps=1, form=FORM_AUTO) -> UpdateRule:
     a, b, c = ns_coef
     return UpdateRule(int(bool(l2norm)), int(muon_steps), float(momentum_beta),
-                      float(a), float(b), float(c))
+                      float(a), float(b), float(c), int(bool(last_layer_only)),
+                      int(inner_steps), int(form))
 
 
 class TTTError(RuntimeError):

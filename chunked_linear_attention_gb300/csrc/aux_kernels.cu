@@ -269,9 +269,9 @@ __global__ void linattn_prefix_kernel(const float* __restrict__ partials,
       const float* p = compact ? partials + (bh * n_upd + u) * (long long)dvdk + e
                                : partials + ((bh * nc + c) * (long long)splits) * dvdk + e;
       for (int sp = 0; sp < splits; ++sp) add += p[(long long)sp * dvdk];
-      const float lr = rule.lr ? rule.lr[bh * nc + c] : 1.f;
+      const float lr = rule.lr ? rule.lr[bh * nc + c] : rule.lr_const;
       if (rule.mom) {
-        m = (rule.alpha ? rule.alpha[bh * nc + c] : 0.f) * m + add;
+        m = (rule.alpha ? rule.alpha[bh * nc + c] : rule.alpha_const) * m + add;
         inc = lr * m;
       } else {
         inc = lr * add;
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(256)
     if (own) {
       const float* p = partials + (((long long)bh * nc + c) * splits) * dvdk + e;
       for (int sp = 0; sp < splits; ++sp) add += p[(long long)sp * dvdk];
-      m = (rule.alpha ? rule.alpha[(long long)bh * nc + c] : 0.f) * m + add;
+      m = (rule.alpha ? rule.alpha[(long long)bh * nc + c] : rule.alpha_const) * m + add;
       x[((long long)bh * n_upd + u) * dvdk + e] = from_f<T>(m);
     }
     float sq = own ? m * m : 0.f;

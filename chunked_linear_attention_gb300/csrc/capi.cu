@@ -53,6 +53,12 @@ int check_layer(int B, int H, int N, int d, int m, int chunk, int io, int mode,
   if (!std::isfinite(rule->momentum_beta) || !std::isfinite(rule->ns_a) ||
       !std::isfinite(rule->ns_b) || !std::isfinite(rule->ns_c))
     return TTT_ERR_ARG;
+  if (rule->last_layer_only != 0 && rule->last_layer_only != 1) return TTT_ERR_ARG;
+  if (rule->inner_steps < 0 || rule->inner_steps > 64) return TTT_ERR_ARG;
+  if (rule->form < TTT_FORM_AUTO || rule->form > TTT_FORM_PARALLEL) return TTT_ERR_ARG;
+  const bool exact_parallel =
+      rule->last_layer_only == 1 && rule->l2norm == 0 && rule->inner_steps <= 1;
+  if (rule->form == TTT_FORM_PARALLEL && !exact_parallel) return TTT_ERR_ARG;
   if (d > 1024 || m > 1024) return TTT_ERR_UNSUPPORTED;
   if (io == TTT_BF16 && (d % 64 != 0 || m % 64 != 0 || chunk % 128 != 0))
     return TTT_ERR_UNSUPPORTED;
@@ -64,6 +70,11 @@ int check_layer(int B, int H, int N, int d, int m, int chunk, int io, int mode,
   D->muon_steps = rule->muon_steps;
   D->beta = rule->momentum_beta;
   D->ns[0] = rule->ns_a; D->ns[1] = rule->ns_b; D->ns[2] = rule->ns_c;
+  D->last_only = rule->last_layer_only;
+  D->inner_steps = rule->inner_steps < 1 ? 1 : rule->inner_steps;
+  D->parallel = exact_parallel && rule->form != TTT_FORM_RECURRENT;
+  if (D->parallel && io == TTT_BF16 && (d > 512 || m > 512)) return TTT_ERR_UNSUPPORTED;
+  if (D->parallel && mode == TTT_STRIDED && N / chunk > 2048) return TTT_ERR_UNSUPPORTED;
   return TTT_OK;
 }
 
@@ -74,7 +85,7 @@ int check_lin(int B, int H, int N, int dk, int dv, int chunk, int io, int mode,
   if (mode < 0 || mode > 3) return TTT_ERR_ARG;
   if (mode == TTT_BIDIRECTIONAL && chunk != N) return TTT_ERR_SHAPE;
   if (io != TTT_F32 && io != TTT_BF16) return TTT_ERR_ARG;
-  if (io == TTT_BF16 && (dk % 64 != 0 || dv % 64 != 0 || dk > 256 || dv > 256 ||
+  if (io == TTT_BF16 && (dk % 64 != 0 || dv % 64 != 0 || dk > 512 || dv > 512 ||
                          chunk % 128 != 0))
     return TTT_ERR_UNSUPPORTED;
   if (io == TTT_F32 && (dk > 1024 || dv > 1024)) return TTT_ERR_UNSUPPORTED;

@@ -3,6 +3,8 @@
 // matching accumulator values of up to three accumulators.
 //
 //   EPI_PROJ_Q   A_q = SiLU(H1) * H3                         (eq 3, queries)
+//                times -eta of the row when eta is given (P of a static
+//                feature map), or the constant a when a != 0
 //   EPI_PROJ_K   dA = -eta * (V W2);  s = sigmoid(H1)
 //                dH1 = dA * H3 * s (1 + H1 (1 - s))  (SiLU', App. I.1)
 //                dH3 = dA * SiLU(H1);  P = -eta * SiLU(H1) * H3
@@ -107,10 +109,13 @@ __device__ __forceinline__ float epilogue_vec(const EpiDesc& e, int z, int r, in
       break;
     }
     case EPI_PROJ_Q: {
+      // optional row factor: -eta of the row (e.eta set) or the constant e.a
+      const float f = e.eta ? -e.eta[(long long)zz * e.eta_z + e.eta_row0 + r]
+                            : (e.a != 0.f ? e.a : 1.0f);
 #pragma unroll
       for (int i = 0; i < V; ++i) {
         const float s = kPrecise ? sigmoid_precise(a0[i]) : sigmoid_f(a0[i]);
-        o[i] = a0[i] * s * a1[i];
+        o[i] = a0[i] * s * a1[i] * f;
       }
       store_vec<WT, V>(static_cast<WT*>(e.out[0]) + idx, o, n);
       break;

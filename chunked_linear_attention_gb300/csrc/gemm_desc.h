@@ -21,7 +21,7 @@ constexpr int kMaxAcc = 3;
 
 enum EpiKind : int {
   EPI_STORE_F32 = 0,   // out0 (fp32) = acc0
-  EPI_PROJ_Q = 1,      // out0 (work) = SiLU(acc0) * acc1                  (A_q)
+  EPI_PROJ_Q = 1,      // out0 (work) = SiLU(acc0) * acc1 (A_q); x (-eta) or x a if set
   EPI_PROJ_K = 2,      // dH1, dH3, P from H1 = acc0, H3 = acc1, VW2 = acc2
   EPI_GRAD = 3,        // M = beta M + acc; U or bf16 X (+ |M|_F^2) from M
   EPI_OUT = 4,         // out0 (io) = acc0

@@ -73,7 +73,31 @@ struct LayerWs {
   float* normsq;       // [3][B*H] squared Frobenius norms of M (per-product paths)
   float* normsq_part;  // [3][B*H][nslot] their partial sums, one per gradient (tile, warp)
   int nslot;
+  // static feature map (W1, W3 fixed): phi(q) and the keys' features for every token
+  void* PhiQ;          // [B*H][N][m]
+  void* PhiK;          // [B*H][N][m]: -eta * phi(k) (recurrent form) or -phi(k) (parallel)
+  void* lin;           // parallel form: the chunked linear attention's workspace
 };
+
+// The chunked linear attention that the parallel form runs: features of
+// width m as keys and queries, values of width d, state W2 [d, m].
+LinDims parallel_lin_dims(const LayerDims& D) {
+  LinDims L;
+  L.B = D.B;
+  L.H = D.H;
+  L.N = D.N;
+  L.dk = D.m;
+  L.dv = D.d;
+  L.chunk = D.chunk;
+  L.bf16 = D.bf16;
+  L.mode = D.mode;
+  L.mom = D.beta != 0.f ? 1 : 0;
+  L.muon_steps = D.muon_steps;
+  L.ns[0] = D.ns[0];
+  L.ns[1] = D.ns[1];
+  L.ns[2] = D.ns[2];
+  return L;
+}
 
 // Partial-sum slots per matrix for the gradient's squared norm: a bound on
 // (output tiles) x (warps per tile) of either GEMM path (tiles at least
@@ -93,12 +117,27 @@ size_t layer_ws_layout(const LayerDims& D, LayerWs* w, char* base) {
   };
   LayerWs tmp;
   LayerWs& o = w ? *w : tmp;
+  std::memset(&o, 0, sizeof(o));
+  if (D.parallel) {
+    // bf16 copies of W1, W3 (the feature map), the features, the linear attention
+    for (int i = 0; i < 2; ++i) o.Wb[i] = D.bf16 ? take(BH * dm * 2) : nullptr;
+    o.PhiQ = take(BH * D.N * D.m * es);
+    o.PhiK = take(BH * D.N * D.m * es);
+    o.lin = take(linattn_workspace_bytes(parallel_lin_dims(D)));
+    return off;
+  }
+  if (D.last_only) {
+    o.PhiQ = take(BH * D.N * D.m * es);
+    o.PhiK = take(BH * D.N * D.m * es);
+  }
   for (int i = 0; i < 3; ++i) o.Wb[i] = D.bf16 ? take(BH * dm * 2) : nullptr;
   for (int i = 0; i < 3; ++i) o.Wb2[i] = D.bf16 ? take(BH * dm * 2) : nullptr;
-  o.Aq = take(BH * D.chunk * D.m * es);
-  o.dH1 = take(BH * D.chunk * D.m * es);
-  o.dH3 = take(BH * D.chunk * D.m * es);
-  o.P = take(BH * D.chunk * D.m * es);
+  if (!D.last_only) {   // per-chunk activations (the static feature map has them all)
+    o.Aq = take(BH * D.chunk * D.m * es);
+    o.dH1 = take(BH * D.chunk * D.m * es);
+    o.dH3 = take(BH * D.chunk * D.m * es);
+    o.P = take(BH * D.chunk * D.m * es);
+  }
   o.M = D.beta != 0.f ? reinterpret_cast<float*>(take(3 * BH * dm * 4)) : nullptr;
   o.U = reinterpret_cast<float*>(take(3 * BH * dm * 4));
   if (D.muon_steps > 0) {
@@ -159,7 +198,7 @@ struct LayerPlan {
   LayerWs w;
   MatSet ms[3];
   float* mom[3];
-  TensorRef Tq, Tk, Tv, TW[2][3], TAq, TdH1, TdH3, TP;
+  TensorRef Tq, Tk, Tv, TW[2][3], TAq, TdH1, TdH3, TP, TPhiQ, TPhiK;
   void* wb[2][3];   // the two bf16 copies of the weights (both the first when there is one)
   std::vector<std::pair<int, int>> steps;
   int* status;
@@ -227,6 +266,44 @@ struct ApplyEvents {
   cudaEvent_t ev_a[2];
 };
 
+// The static feature map of the last-layer-only forms ("Test-Time Training
+// with KV Binding Is Secretly Linear Attention", sec. 6.1 Step 1, App. H):
+// phi(x) = SiLU(x W1^T) o (x W3^T) for every token of every sequence, in one
+// launch: queries -> PhiQ, keys -> PhiK scaled by -eta per token (recurrent
+// form: P of the W2 gradient, g2 = V^T P) or by -1 (parallel form: the
+// linear attention's keys, so that its state increment is the gradient).
+int enqueue_featurize(const LayerPlan& L, MapCache& cache, bool keys_eta, cudaStream_t st) {
+  const LayerArgs& a = *L.a;
+  const LayerDims& D = *L.D;
+  const int BH = D.B * D.H, N = D.N, d = D.d, m = D.m;
+  LaunchBuilder LB(D.bf16, &cache, L.status, L.wait_ns);
+  const int BM = LB.bm();
+  const int bn = LB.choose_bn(m, 2);
+  for (int which = 0; which < 2; ++which) {
+    Problem p = prob0(N, m, d, BH, 2, bn);
+    p.a[0] = LB.op(which == 0 ? L.Tq : L.Tk, 0, 0, N, BM);
+    p.b[0] = LB.op(L.TW[0][0], 0, 0, m, bn);
+    p.a[1] = p.a[0];
+    p.b[1] = LB.op(L.TW[0][1], 0, 0, m, bn);
+    p.a_shared = 1 << 1;
+    p.epi.kind = EPI_PROJ_Q;
+    p.epi.out[0] = which == 0 ? L.w.PhiQ : L.w.PhiK;
+    p.epi.out_ld = m;
+    p.epi.out_z = (long long)N * m;
+    if (which == 1) {
+      if (keys_eta) {
+        p.epi.eta = a.eta;
+        p.epi.eta_z = N;
+      } else {
+        p.epi.a = -1.f;
+      }
+    }
+    LB.add(p);
+  }
+  if (!LB.ok()) return -4;
+  return LB.launch(st, PT_FEATURIZE) == cudaSuccess ? 0 : -6;
+}
+
 int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStream_t st,
                   const IoHooks* io = nullptr,
                   cudaStream_t sa = nullptr, const ApplyEvents* aev = nullptr) {
@@ -238,6 +315,7 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
   const long long dm = (long long)d * m;
   const int rows_of[3] = {m, m, d}, cols_of[3] = {d, d, m};
   const bool muon = D.muon_steps > 0;
+  const bool lo = D.last_only != 0;   // only W2 updates; features precomputed
   const size_t es = tc ? 2 : 4;
   const size_t ios = tc ? 2 : 4;
   auto offs = [&](void* p, long long elems) -> void* {
@@ -278,7 +356,7 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
   auto add_apply_out = [&](int ap) {
     const int bn = LB.choose_bn(d, 1);
     Problem p = prob0(b, d, m, nh, 1, bn);
-    p.a[0] = LB.op(L.TAq, 0, h0 * b, b, BM);
+    p.a[0] = lo ? LB.op(L.TPhiQ, 0, h0 * N + ap * b, N, BM) : LB.op(L.TAq, 0, h0 * b, b, BM);
     p.b[0] = LB.op(L.TW[cur][2], 0, h0 * d, d, bn);  // W2 [d, m]: N = d rows, K = m contiguous
     p.kd = (tc && m % 128 == 0) ? 2 : 1;   // same stage size as the gradients
     p.epi.kind = EPI_OUT;
@@ -312,9 +390,11 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
     if (split && ap >= 0) {
       TTT_CK(cudaStreamWaitEvent(sa, aev->ev_w, 0));
       if (io) TTT_CK(cudaStreamWaitEvent(sa, io->in_ev[std::min(ap, io->n_in - 1)], 0));
-      add_apply_proj(ap);
-      if (!LB.ok()) return -4;
-      TTT_CK(LB.launch(sa, PT_APPLY_PROJ, 0, apply_ctas(nh, D.muon_steps, D)));
+      if (!lo) {
+        add_apply_proj(ap);
+        if (!LB.ok()) return -4;
+        TTT_CK(LB.launch(sa, PT_APPLY_PROJ, 0, apply_ctas(nh, D.muon_steps, D)));
+      }
       add_apply_out(ap);
       if (!LB.ok()) return -4;
       TTT_CK(LB.launch(sa, PT_APPLY_OUT, 0, apply_ctas(nh, D.muon_steps, D)));
@@ -325,8 +405,8 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
       TTT_CK(cudaEventRecord(aev->ev_a[cur], sa));
       apply_reads[cur] = true;
     }
-    // ---------------- PROJ
-    if (up >= 0) {
+    // ---------------- PROJ (not with the static feature map: P is precomputed)
+    if (up >= 0 && !lo) {
       const int bn = LB.choose_bn(m, 3);
       Problem p = prob0(b, m, d, nh, 3, bn);
       p.a[0] = LB.op(L.Tk, 0, h0 * N + up * b, N, BM);
@@ -347,15 +427,15 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
       p.epi.eta_row0 = (long long)up * b;
       LB.add(p);
     }
-    if (!split && ap >= 0) add_apply_proj(ap);
-    if (up >= 0 || (!split && ap >= 0)) {
+    if (!split && ap >= 0 && !lo) add_apply_proj(ap);
+    if (!lo && (up >= 0 || (!split && ap >= 0))) {
       if (!LB.ok()) return -4;
       TTT_CK(LB.launch(st, PT_PROJ, gprio));
     }
 
     // ---------------- GRAD (+ OUT)
     if (up >= 0) {
-      for (int s = 0; s < 3; ++s) {
+      for (int s = lo ? 2 : 0; s < 3; ++s) {
         const int M = rows_of[s], Nn = cols_of[s];
         const int bn = LB.choose_bn(Nn, 1);
         Problem p = prob0(M, Nn, b, nh, 1, bn);
@@ -366,7 +446,8 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
           p.b[0] = LB.op(L.Tk, 1, h0 * N + up * b, N, 64, 64 * kdg);
         } else {      // g2 = V^T P  [d, m]
           p.a[0] = LB.op(L.Tv, 1, h0 * N + up * b, N, 64, 64 * kdg);
-          p.b[0] = LB.op(L.TP, 1, h0 * b, b, 64, 64 * kdg);
+          p.b[0] = lo ? LB.op(L.TPhiK, 1, h0 * N + up * b, N, 64, 64 * kdg)
+                      : LB.op(L.TP, 1, h0 * b, b, 64, 64 * kdg);
         }
         p.kd = kdg;
         p.epi.kind = EPI_GRAD;
@@ -428,6 +509,8 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
       na.ns[1] = D.ns[1];
       na.ns[2] = D.ns[2];
       na.priority = prio;
+      na.slot0 = lo ? 2 : 0;
+      na.nslots = lo ? 1 : 3;
       int rc = 1;
       if (use_ns_half(d)) rc = launch_ns_half(cache, na, L.status, L.wait_ns, st);
       if (rc == 1) {
@@ -444,8 +527,13 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
       const long long ss = (long long)sdim * sdim;
       // groups of equally shaped slots: {0,1,2} if square, else {0,1} and {2}
       NsGroup groups[2];
-      const int gfirst[2] = {0, 2}, gcount[2] = {d == m ? 3 : 2, 1};
-      const int ng = d == m ? 1 : 2;
+      int gfirst[2] = {0, 2}, gcount[2] = {d == m ? 3 : 2, 1};
+      int ng = d == m ? 1 : 2;
+      if (lo) {   // W2 alone
+        gfirst[0] = 2;
+        gcount[0] = 1;
+        ng = 1;
+      }
       for (int g = 0; g < ng; ++g) {
         const int s0 = gfirst[g];
         NsGroup& q = groups[g];
@@ -473,8 +561,9 @@ int enqueue_range(const LayerPlan& L, MapCache& cache, int h0, int nh, cudaStrea
         part[s].work = L.wb[nxt][s] ? static_cast<char*>(L.wb[nxt][s]) + h0 * rc * 2 : nullptr;
         part[s].update = L.ms[s].update + h0 * rc;
       }
-      ProfScope ps(PT_NORM, st, 0.0, 3.0 * nh * dm * (4 + 4 + 4 + (tc ? 2 : 0)));
-      TTT_CK(launch_update_normalize(part, 3, nh, D.l2norm, st));
+      const int s_first = lo ? 2 : 0, ns_ = 3 - s_first;
+      ProfScope ps(PT_NORM, st, 0.0, (double)ns_ * nh * dm * (4 + 4 + 4 + (tc ? 2 : 0)));
+      TTT_CK(launch_update_normalize(part + s_first, ns_, nh, D.l2norm, st));
     }
     cur = nxt;
     if (split) TTT_CK(cudaEventRecord(aev->ev_w, st));
@@ -620,6 +709,11 @@ int enqueue_all(LayerPlan& L, cudaStream_t st) {
                              3LL * BH * (1 + w.nslot), st));
   }
   MapCache cache;
+  if (D.last_only) {   // the static feature map's outputs for every token, once
+    if (hio) TTT_CK(cudaStreamWaitEvent(st, chunk_ev[nc - 1], 0));
+    const int rc = enqueue_featurize(L, cache, true, st);
+    if (rc != 0) return rc;
+  }
   if (ng > 1) {
     std::vector<cudaStream_t> kids(pool.begin(), pool.begin() + ng);
     TTT_CK(fork_streams(st, kids));
@@ -646,6 +740,87 @@ int enqueue_all(LayerPlan& L, cudaStream_t st) {
                              cudaMemcpyDeviceToHost, st));
     std::vector<cudaStream_t> io(pool.begin() + io0, pool.begin() + io0 + 1 + ng);
     TTT_CK(join_streams(st, io));
+  }
+  return 0;
+}
+
+// The parallel form ("Test-Time Training with KV Binding Is Secretly Linear
+// Attention", sec. 6.2 and App. H; Variant 2): with W1, W3 static and no
+// normalisation the W2 update is associative, so the scan becomes
+//   1. the features phi(q), phi(k) of every token (one launch),
+//   2. chunked linear attention with phi(q) as queries, -phi(k) as keys, v
+//      and eta as values and rates, state W2 [d, m]: per updating chunk
+//      M <- beta M + G with G = (eta v)^T (-phi(k)) = g2 (the W2 gradient),
+//      W2 <- W2 + (-1) Muon(M) (or M), and O = W2 phi(q) in mask order.
+// Host-buffer calls copy all inputs in first and the results out after.
+int enqueue_parallel(LayerPlan& L, cudaStream_t st) {
+  const LayerArgs& a = *L.a;
+  const LayerDims& D = *L.D;
+  const LayerWs& w = L.w;
+  const HostIO* hio = a.host;
+  const int BH = D.B * D.H;
+  const long long dm = (long long)D.d * D.m;
+  const size_t ios = D.bf16 ? 2 : 4;
+  const size_t act = (size_t)BH * D.N * D.d * ios;
+  float* mom2 = a.momentum ? a.momentum + (long long)BH * dm : nullptr;   // M2 of (M1, M2, M3)
+  if (hio) {
+    const void* src[3] = {hio->q, hio->k, hio->v};
+    const void* dst[3] = {a.q, a.k, a.v};
+    for (int i = 0; i < 3; ++i) {
+      if (i == 1 && hio->k == hio->q) continue;
+      TTT_CK(cudaMemcpyAsync(const_cast<void*>(dst[i]), src[i], act, cudaMemcpyHostToDevice, st));
+    }
+    TTT_CK(cudaMemcpyAsync(const_cast<float*>(a.eta), hio->eta, (size_t)BH * D.N * 4,
+                           cudaMemcpyHostToDevice, st));
+    const size_t wrows = (size_t)(a.w_per_batch ? D.B : 1) * D.H;
+    for (int s = 0; s < 3; ++s)
+      TTT_CK(cudaMemcpyAsync(const_cast<float*>(a.W[s]), hio->W[s], wrows * dm * 4,
+                             cudaMemcpyHostToDevice, st));
+    if (hio->momentum)
+      TTT_CK(cudaMemcpyAsync(a.momentum, hio->momentum, 3 * (size_t)BH * dm * 4,
+                             cudaMemcpyHostToDevice, st));
+  }
+  {
+    // final weights = initial ones (W1, W3 stay; W2 is the linear attention's
+    // initial state), bf16 copies of W1 and W3 for the feature map
+    MatSet ms[3];
+    for (int s = 0; s < 3; ++s) {
+      ms[s] = L.ms[s];
+      ms[s].work = s < 2 ? w.Wb[s] : nullptr;
+    }
+    ProfScope ps(PT_INIT, st, 0.0, 3.0 * BH * dm * (4 + 4) + 2.0 * BH * dm * (D.bf16 ? 2 : 0));
+    TTT_CK(launch_init_layer(ms, 3, D.B, D.H, nullptr, 0, nullptr, 0, st));
+  }
+  MapCache cache;
+  int rc = enqueue_featurize(L, cache, false, st);
+  if (rc != 0) return rc;
+  LinDims LD = parallel_lin_dims(D);
+  LD.mom = (D.beta != 0.f || mom2) ? 1 : 0;
+  LinArgs la;
+  la.q = w.PhiQ;
+  la.k = w.PhiK;
+  la.v = a.v;
+  la.eta = a.eta;
+  la.S0 = a.Wf[1];
+  la.update_chunks = a.update_chunks;
+  la.out = a.out;
+  la.S_final = a.Wf[1];
+  la.workspace = w.lin;
+  la.stream = st;
+  la.M0 = mom2;
+  la.M_final = mom2;
+  la.alpha_const = D.beta;
+  la.lr_const = -1.f;
+  rc = linattn_forward(la, LD, L.status, L.wait_ns);
+  if (rc != 0) return rc;
+  if (hio) {
+    TTT_CK(cudaMemcpyAsync(hio->out, a.out, act, cudaMemcpyDeviceToHost, st));
+    for (int s = 0; s < 3; ++s)
+      TTT_CK(cudaMemcpyAsync(hio->Wf[s], a.Wf[s], (size_t)BH * dm * 4, cudaMemcpyDeviceToHost,
+                             st));
+    if (hio->momentum)
+      TTT_CK(cudaMemcpyAsync(hio->momentum, a.momentum, 3 * (size_t)BH * dm * 4,
+                             cudaMemcpyDeviceToHost, st));
   }
   return 0;
 }
@@ -695,6 +870,14 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
       L.TW[c][s] = TensorRef{tc ? L.wb[c][s] : static_cast<const void*>(a.Wf[kPub[s]]), wb16,
                              (long long)BH * rows_of[s], cols_of[s]};
   }
+  if (D.last_only) {   // W1, W3 never change: both bf16 copies are the first
+    L.wb[1][0] = L.wb[0][0];
+    L.wb[1][1] = L.wb[0][1];
+    for (int s = 0; s < 2; ++s)
+      L.TW[1][s] = L.TW[0][s];
+  }
+  L.TPhiQ = TensorRef{w.PhiQ, wb16, (long long)BH * N, m};
+  L.TPhiK = TensorRef{w.PhiK, wb16, (long long)BH * N, m};
   L.TAq = TensorRef{w.Aq, wb16, (long long)BH * b, m};
   L.TdH1 = TensorRef{w.dH1, wb16, (long long)BH * b, m};
   L.TdH3 = TensorRef{w.dH3, wb16, (long long)BH * b, m};
@@ -702,8 +885,14 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
 
   // step schedule: (apply chunk, update chunk), -1 = none
   std::vector<uint64_t> flagbits((nc + 63) / 64, 0);
+  // (inner_steps > 1: the update of a chunk repeated on the same chunk, the
+  // apply reading the weights before the first (apply-then-update) or after
+  // the last repetition)
   if (D.mode == 0) {
-    for (int c = 0; c < nc; ++c) L.steps.push_back({c, c});
+    for (int c = 0; c < nc; ++c) {
+      L.steps.push_back({c, c});
+      for (int r = 1; r < D.inner_steps; ++r) L.steps.push_back({-1, c});
+    }
   } else {
     std::vector<int> pending;
     for (int c = 0; c < nc; ++c) {
@@ -715,6 +904,7 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
           pending.erase(pending.begin());
         }
         L.steps.push_back({pending.empty() ? -1 : pending.front(), c});
+        for (int r = 1; r < D.inner_steps; ++r) L.steps.push_back({-1, c});
         pending.assign(1, c);
       } else {
         pending.push_back(c);
@@ -734,7 +924,8 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
       (uint64_t)D.chunk, (uint64_t)D.bf16, (uint64_t)D.mode, (uint64_t)D.l2norm,
       (uint64_t)D.muon_steps, fbits(D.beta),
       fbits(D.ns[0]), fbits(D.ns[1]),
-      fbits(D.ns[2]), (uint64_t)status, (uint64_t)wait_ns};
+      fbits(D.ns[2]), (uint64_t)status, (uint64_t)wait_ns, (uint64_t)D.last_only,
+      (uint64_t)D.inner_steps, (uint64_t)D.parallel};
   key.insert(key.end(), flagbits.begin(), flagbits.end());
   if (a.host) {   // host-buffer call: the host tensors too
     const HostIO& h = *a.host;
@@ -746,6 +937,10 @@ int layer_forward(const LayerArgs& a, const LayerDims& D, int* status,
   }
   // one-time device setup outside any capture
   high_priority();
+  if (D.parallel) {   // a few launches; the linear attention's own setup runs on the way
+    if (tc && prepare_umma_gemm() != cudaSuccess) return -6;
+    return enqueue_parallel(L, a.stream);
+  }
   if (tc) {
     if (prepare_umma_gemm() != cudaSuccess) return -6;
     if (muon && d == m) {

@@ -16,6 +16,9 @@ struct LayerDims {
   int muon_steps;
   float beta;
   float ns[3];
+  int last_only = 0;     // only W2 updates (W1, W3 static: a static feature map)
+  int inner_steps = 1;   // update steps per updating chunk
+  int parallel = 0;      // the parallel form (last_only, no normalisation, one inner step)
 };
 
 // Page-locked host tensors of a host-buffer call: the layer copies each
@@ -77,6 +80,8 @@ struct LinArgs {
   const float* lr = nullptr;      // [B*H][nc] learning rate per chunk, or NULL (1)
   const float* M0 = nullptr;      // [B*H][dv*dk] initial momentum, or NULL (zeros)
   float* M_final = nullptr;       // [B*H][dv*dk] final momentum, or NULL
+  float alpha_const = 0.f;        // alpha of every chunk when alpha is NULL
+  float lr_const = 1.f;           // learning rate of every chunk when lr is NULL
 };
 
 size_t linattn_workspace_bytes(const LinDims& D);

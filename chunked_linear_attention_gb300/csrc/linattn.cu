@@ -146,6 +146,8 @@ int linattn_forward(const LinArgs& a, const LinDims& D, int* status, unsigned lo
   rule.M0 = a.M0;
   rule.M_final = a.M_final;
   rule.mom = D.mom;
+  rule.alpha_const = a.alpha_const;
+  rule.lr_const = a.lr_const;
   const bool muon = D.muon_steps > 0;
 
   if (!muon && linattn_fused_applicable(D)) {
@@ -208,7 +210,7 @@ int linattn_forward(const LinArgs& a, const LinDims& D, int* status, unsigned lo
                               D.mode == 0, flags, rule, 0, n_upd, tc, st) != cudaSuccess)
       return -6;
   } else if (n_upd == 0) {   // nothing updates: every chunk reads S0
-    LinRule none = {};
+    LinRule none;
     if (launch_linattn_prefix(w.partials, a.S0, w.Sread, a.S_final, BH, nc, splits, dvdk,
                               D.mode == 0, flags, none, 0, 0, tc, st) != cudaSuccess)
       return -6;
@@ -240,8 +242,9 @@ int linattn_forward(const LinArgs& a, const LinDims& D, int* status, unsigned lo
     LB.reset();
     const int rc = enqueue_ns_products(LB, &g, 1, D.muon_steps, D.ns, st);
     if (rc != 0) return rc;
-    LinRule upd_rule = {};
+    LinRule upd_rule;
     upd_rule.lr = a.lr;
+    upd_rule.lr_const = a.lr_const;
     ProfScope ps(PT_LIN_PREFIX, st, 0.0, (double)BH * nc * dvdk * (4.0 + (tc ? 2 : 4)));
     if (launch_linattn_prefix(w.U, a.S0, w.Sread, a.S_final, BH, nc, 1, dvdk, D.mode == 0, flags,
                               upd_rule, 1, n_upd, tc, st) != cudaSuccess)

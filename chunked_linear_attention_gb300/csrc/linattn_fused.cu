@@ -206,8 +206,9 @@ __device__ __forceinline__ void prefix_item(const LinFusedLaunch& L, int bh, int
         // chunk pr / splits complete: the state it reads, then the running state
         const int c = pr / L.splits;
         const bool upd = chunk_updates(L, c);
-        const float lr = (upd && R.lr) ? R.lr[(long long)bh * L.nc + c] : 1.f;
-        const float al = (upd && R.mom && R.alpha) ? R.alpha[(long long)bh * L.nc + c] : 0.f;
+        const float lr = (upd && R.lr) ? R.lr[(long long)bh * L.nc + c] : R.lr_const;
+        const float al = (upd && R.mom && R.alpha) ? R.alpha[(long long)bh * L.nc + c]
+                                                   : R.alpha_const;
 #pragma unroll
         for (int g = 0; g < kPG; ++g) {
           if (!own[g]) continue;

@@ -19,13 +19,16 @@ struct UpdateFlags {
 // Training with KV Binding Is Secretly Linear Attention", Thm 5.3, App. H):
 // per updating chunk c, M <- alpha_c M + G_c and S <- S + lr_c M (or, with
 // mom = 0, S <- S + lr_c G_c).  alpha / lr are [BH][nc] (NULL: alpha = 0,
-// lr = 1); M0 / M_final are [BH][dv*dk] fp32 (NULL: zeros / not written).
+// lr = 1, or the constants below); M0 / M_final are [BH][dv*dk] fp32 (NULL:
+// zeros / not written).
 struct LinRule {
-  const float* alpha;
-  const float* lr;
-  const float* M0;
-  float* M_final;
-  int mom;
+  const float* alpha = nullptr;
+  const float* lr = nullptr;
+  const float* M0 = nullptr;
+  float* M_final = nullptr;
+  int mom = 0;
+  float alpha_const = 0.f;   // alpha of every chunk when alpha is NULL
+  float lr_const = 1.f;      // learning rate of every chunk when lr is NULL
 };
 
 // vt = eta (per row) * v, in bf16 or fp32.

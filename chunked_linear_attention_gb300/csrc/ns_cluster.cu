@@ -40,6 +40,7 @@ struct NsLaunch {
   void* Wb[3];                // bf16 operand copies per slot
   int BH, d, steps, cs, l2norm;
   int h0, nh;                 // (batch, head) range of this launch
+  int slot0;                  // first matrix slot of this launch
   int* status;
   unsigned long long wait_limit_ns;
 };
@@ -89,7 +90,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int rank = (int)cluster_ctarank();
   // matrix index (slot-major over B*H) of this cluster
   const int zl = blockIdx.x / L.cs;
-  const int z = (zl / L.nh) * L.BH + L.h0 + (zl % L.nh);
+  const int z = (L.slot0 + zl / L.nh) * L.BH + L.h0 + (zl % L.nh);
 
   uint32_t stage_bytes = 0;
   {
@@ -377,6 +378,7 @@ int launch_ns_cluster(MapCache& cache, const NsArgs& a, int* status, unsigned lo
   L.BH = a.BH;
   L.h0 = a.h0;
   L.nh = a.nh;
+  L.slot0 = a.slot0;
   L.d = d;
   L.steps = a.steps;
   L.cs = cs;
@@ -390,14 +392,14 @@ int launch_ns_cluster(MapCache& cache, const NsArgs& a, int* status, unsigned lo
   attr[0].val.clusterDim.x = cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(3 * a.nh * cs, 1, 1);
+  cfg.gridDim = dim3(a.nslots * a.nh * cs, 1, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = kUmmaSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const double r = d, c = d;
-  const double flops = 3.0 * a.nh * a.steps * (4 * r * c * c + 2 * c * c * c);
+  const double flops = (double)a.nslots * a.nh * a.steps * (4 * r * c * c + 2 * c * c * c);
   ProfScope ps(PT_MUON, stream, flops, 0.0);
   if (cudaLaunchKernelEx(&cfg, ns_cluster_kernel, L) != cudaSuccess) return -6;
   return 0;

@@ -19,6 +19,8 @@ struct NsArgs {
   void* Wb[3];       // bf16 operand copies per slot
   int BH, d, steps, l2norm;
   int h0, nh;        // (batch, head) range handled by this launch: [h0, h0 + nh)
+  int slot0 = 0;     // matrix slots handled: [slot0, slot0 + nslots) of (W1, W3, W2)
+  int nslots = 3;
   float ns[3];
   int priority = 0;  // launch priority (0: the stream's own)
 };

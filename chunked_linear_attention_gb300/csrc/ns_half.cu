@@ -67,6 +67,7 @@ struct NsHalfLaunch {
   float* W[3];              // fp32 state per slot (W1, W3, W2), [B*H][d*d]
   void* Wb[3];              // bf16 operand copies per slot
   int BH, d, steps, l2norm, h0, nh, R, nstages;
+  int slot0;                // first matrix slot of this launch (its slots are slot0 ..)
   int mn_split;             // MN-major slices fetched as R shares of 64 columns
   float a, b, c, eps;
   int* status;
@@ -252,7 +253,7 @@ __global__ void __launch_bounds__(kHThreads, 1)
   const uint16_t hmask = (uint16_t)(((1u << R) - 1u) << (h * R));   // CTAs of this half
   const uint16_t pmask = (uint16_t)((1u << rank) | (1u << partner));
   const int zl = blockIdx.x / (2 * R);
-  const int z = (zl / L.nh) * L.BH + L.h0 + (zl % L.nh);
+  const int z = (L.slot0 + zl / L.nh) * L.BH + L.h0 + (zl % L.nh);
   const int mrow = z * d;                     // first row of this matrix in the stacked buffers
   const int prow = mrow + r * 128;            // first row of this CTA's panel
   const unsigned long long lim = L.wait_limit_ns;
@@ -567,6 +568,7 @@ int launch_ns_half(MapCache& cache, const NsArgs& a, int* status, unsigned long 
   L.d = d;
   L.steps = a.steps;
   L.l2norm = a.l2norm;
+  L.slot0 = a.slot0;
   L.h0 = a.h0;
   L.nh = a.nh;
   L.R = R;
@@ -588,17 +590,17 @@ int launch_ns_half(MapCache& cache, const NsArgs& a, int* status, unsigned long 
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   attr[2].id = cudaLaunchAttributePriority;
   attr[2].val.priority = a.priority;
-  cfg.gridDim = dim3(3 * a.nh * cs, 1, 1);
+  cfg.gridDim = dim3(a.nslots * a.nh * cs, 1, 1);
   cfg.blockDim = dim3(kHThreads, 1, 1);
   cfg.dynamicSmemBytes = kUmmaSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = a.priority != 0 ? 3 : 2;
   const double n3 = (double)d * d * d;
-  const double flops = 3.0 * a.nh * a.steps * 6.0 * n3;
+  const double flops = (double)a.nslots * a.nh * a.steps * 6.0 * n3;
   const int sms = device_sm_count();
   ProfScope ps(PT_MUON_HALF, stream, flops, 0.0,
-               sms > 0 ? (double)(3 * a.nh * cs) / sms : 1.0);
+               sms > 0 ? (double)(a.nslots * a.nh * cs) / sms : 1.0);
   if (cudaLaunchKernelEx(&cfg, ns_half_kernel, L) != cudaSuccess) return -6;
   return 0;
 }

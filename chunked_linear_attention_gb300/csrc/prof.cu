@@ -24,13 +24,13 @@ std::vector<Rec> g_recs;
 const char* kTagName[PT_COUNT] = {
     "init", "gemm.proj", "gemm.grad", "gemm.ns_gram", "gemm.ns_poly", "gemm.ns_step",
     "norm", "lin.scale", "gemm.lin_partial", "lin.prefix", "gemm.lin_out", "gemm.selftest", "muon.cluster",
-    "muon.half", "lin.fused", "gemm.apply_proj", "gemm.apply_out"};
+    "muon.half", "lin.fused", "gemm.apply_proj", "gemm.apply_out", "gemm.featurize"};
 const char* kTagKernel[PT_COUNT] = {
     "init_layer_kernel", "umma_gemm_kernel", "umma_gemm_kernel", "umma_gemm_kernel",
     "umma_gemm_kernel", "umma_gemm_kernel", "update_normalize_kernel", "scale_rows_kernel",
     "umma_gemm_kernel", "linattn_prefix_kernel", "umma_gemm_kernel", "umma_gemm_kernel",
     "ns_cluster_kernel", "ns_half_kernel", "linattn_fused_kernel",
-    "umma_gemm_kernel", "umma_gemm_kernel"};
+    "umma_gemm_kernel", "umma_gemm_kernel", "umma_gemm_kernel"};
 
 }  // namespace
 

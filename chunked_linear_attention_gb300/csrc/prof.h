@@ -24,6 +24,7 @@ enum ProfTag : int {
   PT_LIN_FUSED,
   PT_APPLY_PROJ,
   PT_APPLY_OUT,
+  PT_FEATURIZE,
   PT_COUNT
 };
 

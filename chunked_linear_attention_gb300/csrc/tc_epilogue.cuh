@@ -324,8 +324,10 @@ __device__ __noinline__ float tc_epilogue_blocks(const Problem& P, int tn, uint3
       store_rows<float, BW, V8>(v0, st, static_cast<float*>(e.out[0]) + off, e.out_ld, rows_valid,
                             lane);
     } else if constexpr (KIND == EPI_PROJ_Q) {
+      // optional row factor: -eta of the row (e.eta set) or the constant e.a
+      const float f = e.eta ? -eta : (e.a != 0.f ? e.a : 1.0f);
 #pragma unroll
-      for (int i = 0; i < BW; ++i) v0[i] = v0[i] * sigmoid_f(v0[i]) * v1[i];
+      for (int i = 0; i < BW; ++i) v0[i] = v0[i] * sigmoid_f(v0[i]) * v1[i] * f;
       store_rows<__nv_bfloat16, BW, V8>(v0, st, static_cast<__nv_bfloat16*>(e.out[0]) + off, e.out_ld,
                                     rows_valid, lane);
     } else if constexpr (KIND == EPI_PROJ_K) {
@@ -404,7 +406,7 @@ __device__ __forceinline__ float tc_epilogue_tile(const Problem& P, int z, int t
   const int c_begin = 16 * (slice * nblk / kSplit), c_end = 16 * ((slice + 1) * nblk / kSplit);
 
   float eta = 0.f, scale = 1.f;
-  if (e.kind == EPI_PROJ_K && myrow < P.M)
+  if ((e.kind == EPI_PROJ_K || (e.kind == EPI_PROJ_Q && e.eta)) && myrow < P.M)
     eta = e.eta[(long long)zz * e.eta_z + e.eta_row0 + myrow];
   if ((e.kind == EPI_NS_GRAM || e.kind == EPI_NS_STEP || (e.kind == EPI_NS_POLY && e.in_tmem)) &&
       e.first)

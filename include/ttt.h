@@ -72,13 +72,36 @@ typedef enum {
   TTT_STRIDED = 3
 } ttt_mask_mode;
 
+/* Forms of the chunk scan (form field of ttt_update_rule). */
+typedef enum {
+  TTT_FORM_AUTO = 0,       /* parallel where it is exact (see below), else recurrent */
+  TTT_FORM_RECURRENT = 1,  /* chunk after chunk */
+  TTT_FORM_PARALLEL = 2    /* the parallel form; TTT_ERR_ARG where it is not exact */
+} ttt_form;
+
 /* Weight-update rule ("5.2.1 LaCT and TTT-E2E", eqs (5), (6) and the
  * momentum sentence after eq (6)).
- *   l2norm        : 1 = L2-Normalize every row of W1, W2, W3 after W - U.
+ *   l2norm        : 1 = L2-Normalize every updated row after W - U.
  *   muon_steps    : Newton-Schulz steps of Muon(M); 0 = U is M itself.
  *   momentum_beta : M <- beta M + g; 0 = no momentum (M = g).
  *   ns_a/ns_b/ns_c: Newton-Schulz coefficients X <- aX + b(XX^T)X + c(XX^T)^2X
  *                   (the Muon quintic is 3.4445, -4.7750, 2.0315).
+ *   last_layer_only: 1 = only W2 updates; W1 and W3 keep their initial
+ *                   values, so phi(x) = SiLU(W1 x) o (W3 x) is a static
+ *                   feature map ("Test-Time Training with KV Binding Is
+ *                   Secretly Linear Attention", sec. 6.1 Step 1, Variant 1).
+ *   inner_steps   : update steps taken on each updating chunk (each one a
+ *                   gradient at the current weights, momentum, Muon and
+ *                   normalisation); 0 or 1 = one ("Test-Time Training with
+ *                   KV Binding...", sec. 4.1 / Fig. 1, more inner-loop steps).
+ *   form          : ttt_form.  The parallel form (App. H, sec. 6.2: static
+ *                   feature map, no normalisation, so the state update is
+ *                   associative; Variant 2) is exact when last_layer_only = 1,
+ *                   l2norm = 0 and inner_steps <= 1; it first computes phi(q)
+ *                   and phi(k) for every token, then runs the chunked linear
+ *                   attention with momentum and Muon of
+ *                   linattn_chunked_forward_rule (needs d_h, m_h <= 512 on
+ *                   the bf16 path).
  * Muon first scales M to unit Frobenius norm (eps 1e-7) and transposes a
  * matrix with more rows than columns. */
 typedef struct {
@@ -86,6 +109,9 @@ typedef struct {
   int muon_steps;
   float momentum_beta;
   float ns_a, ns_b, ns_c;
+  int last_layer_only;
+  int inner_steps;
+  int form;
 } ttt_update_rule;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -190,7 +216,7 @@ size_t linattn_workspace_size(int B, int H, int N, int d_k, int d_v, int chunk,
  *   S_final     fp32 [B, H, d_v, d_k] state after the last chunk (may be NULL).
  *   workspace   at least linattn_workspace_size() bytes, 256-byte aligned.
  *
- * Supported: io_dtype TTT_BF16 with d_k, d_v multiples of 64 (<= 256) and
+ * Supported: io_dtype TTT_BF16 with d_k, d_v multiples of 64 (<= 512) and
  * chunk a multiple of 128; io_dtype TTT_F32 with d_k, d_v <= 1024. */
 int linattn_chunked_forward(const void* q, const void* k, const void* v, const float* eta,
                             const float* S0, int B, int H, int N, int d_k, int d_v,
