@@ -269,7 +269,7 @@ __global__ void linattn_prefix_kernel(const float* __restrict__ partials,
       const float* p = compact ? partials + (bh * n_upd + u) * (long long)dvdk + e
                                : partials + ((bh * nc + c) * (long long)splits) * dvdk + e;
       for (int sp = 0; sp < splits; ++sp) add += p[(long long)sp * dvdk];
-      const float lr = rule.lr ? rule.lr[bh * nc + c] : rule.lr_const;
+      const float lr = (rule.lr ? rule.lr[bh * nc + c] : rule.lr_const) * rule.inc_scale;
       if (rule.mom) {
         m = (rule.alpha ? rule.alpha[bh * nc + c] : rule.alpha_const) * m + add;
         inc = lr * m;

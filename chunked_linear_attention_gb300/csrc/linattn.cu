@@ -18,6 +18,7 @@
 #include "layer.h"
 #include "linattn_fused.h"
 #include "linattn_kernels.h"
+#include "ns_half.h"
 #include "ns_products.h"
 #include "prof.h"
 
@@ -55,6 +56,7 @@ struct LinWs {
   void* G;
   void* Bm;
   float* U;
+  void* Ub;            // bf16 copy the half-panel kernel writes beside U (unused)
   float* normsq;
   float* norm_part;
   int nslot;
@@ -87,10 +89,11 @@ size_t lin_layout(const LinDims& D, LinWs* w, char* base) {
     o.G = take(Z * sm * sm * es);
     o.Bm = take(Z * sm * sm * es);
     o.U = reinterpret_cast<float*>(take(Z * E * 4));
+    o.Ub = take(Z * E * 2);
     o.normsq = reinterpret_cast<float*>(take(Z * 4));
     o.norm_part = reinterpret_cast<float*>(take(Z * o.nslot * 4));
   } else {
-    o.X[0] = o.X[1] = o.G = o.Bm = nullptr;
+    o.X[0] = o.X[1] = o.G = o.Bm = o.Ub = nullptr;
     o.U = o.normsq = o.norm_part = nullptr;
   }
   return off;
@@ -228,23 +231,61 @@ int linattn_forward(const LinArgs& a, const LinDims& D, int* status, unsigned lo
         return -6;
     }
     const int Z = BH * n_upd;
-    if (launch_normsq_sum(w.norm_part, w.nslot, w.normsq, Z, st) != cudaSuccess) return -6;
-    NsGroup g;
-    g.X[0] = w.X[0];
-    g.X[1] = w.X[1];
-    g.G = w.G;
-    g.Bm = w.Bm;
-    g.U = w.U;
-    g.normsq = w.normsq;
-    g.Z = Z;
-    g.R = dv;
-    g.C = dk;
-    LB.reset();
-    const int rc = enqueue_ns_products(LB, &g, 1, D.muon_steps, D.ns, st);
-    if (rc != 0) return rc;
+    float sign = 1.f;
+    int rc = 1;
+    if (tc && dv == dk && ns_half_applicable(dv) && prepare_ns_half(dv)) {
+      // all updates through the half-panel cluster kernel: its update step
+      // W <- W - Muon(M) without normalisation, over a zeroed fp32 W, leaves
+      // -Muon(M_u) in U (its bf16 copy goes to Ub)
+      if (cudaMemsetAsync(w.U, 0, (size_t)Z * dvdk * 4, st) != cudaSuccess) return -6;
+      NsArgs na;
+      na.X[0] = w.X[0];
+      na.X[1] = w.X[1];
+      na.G = w.G;
+      na.Bm = w.Bm;
+      na.U = nullptr;
+      na.normsq = w.normsq;
+      na.normsq_part = w.norm_part;
+      na.nslot = w.nslot;
+      for (int s = 0; s < 3; ++s) {
+        na.W[s] = w.U;
+        na.Wb[s] = w.Ub;
+      }
+      na.BH = Z;
+      na.d = dv;
+      na.steps = D.muon_steps;
+      na.l2norm = 0;
+      na.h0 = 0;
+      na.nh = Z;
+      for (int i = 0; i < 3; ++i) na.ns[i] = D.ns[i];
+      na.slot0 = 0;
+      na.nslots = 1;
+      na.zcount = Z;
+      MapCache ncache;
+      rc = launch_ns_half(ncache, na, status, wait_ns, st);
+      if (rc < 0) return rc;
+      if (rc == 0) sign = -1.f;
+    }
+    if (rc != 0) {   // the per-product launches
+      if (launch_normsq_sum(w.norm_part, w.nslot, w.normsq, Z, st) != cudaSuccess) return -6;
+      NsGroup g;
+      g.X[0] = w.X[0];
+      g.X[1] = w.X[1];
+      g.G = w.G;
+      g.Bm = w.Bm;
+      g.U = w.U;
+      g.normsq = w.normsq;
+      g.Z = Z;
+      g.R = dv;
+      g.C = dk;
+      LB.reset();
+      rc = enqueue_ns_products(LB, &g, 1, D.muon_steps, D.ns, st);
+      if (rc != 0) return rc;
+    }
     LinRule upd_rule;
     upd_rule.lr = a.lr;
     upd_rule.lr_const = a.lr_const;
+    upd_rule.inc_scale = sign;
     ProfScope ps(PT_LIN_PREFIX, st, 0.0, (double)BH * nc * dvdk * (4.0 + (tc ? 2 : 4)));
     if (launch_linattn_prefix(w.U, a.S0, w.Sread, a.S_final, BH, nc, 1, dvdk, D.mode == 0, flags,
                               upd_rule, 1, n_upd, tc, st) != cudaSuccess)

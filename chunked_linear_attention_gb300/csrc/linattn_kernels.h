@@ -29,6 +29,7 @@ struct LinRule {
   int mom = 0;
   float alpha_const = 0.f;   // alpha of every chunk when alpha is NULL
   float lr_const = 1.f;      // learning rate of every chunk when lr is NULL
+  float inc_scale = 1.f;     // factor of every increment (the sign of a negated Muon output)
 };
 
 // vt = eta (per row) * v, in bf16 or fp32.

@@ -21,6 +21,7 @@ struct NsArgs {
   int h0, nh;        // (batch, head) range handled by this launch: [h0, h0 + nh)
   int slot0 = 0;     // matrix slots handled: [slot0, slot0 + nslots) of (W1, W3, W2)
   int nslots = 3;
+  int zcount = 0;    // matrices in X / G (tensor-map extents); 0 = 3 * BH
   float ns[3];
   int priority = 0;  // launch priority (0: the stream's own)
 };

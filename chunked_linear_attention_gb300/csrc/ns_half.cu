@@ -535,7 +535,7 @@ bool prepare_ns_half(int d) {
 int launch_ns_half(MapCache& cache, const NsArgs& a, int* status, unsigned long long wait_ns,
                    cudaStream_t stream) {
   if (!prepare_ns_half(a.d) || a.steps < 1) return 1;
-  const int d = a.d, R = d / 128, cs = 2 * R, Z = 3 * a.BH;
+  const int d = a.d, R = d / 128, cs = 2 * R, Z = a.zcount > 0 ? a.zcount : 3 * a.BH;
   NsHalfLaunch L;
   std::memset(&L, 0, sizeof(L));
   const TensorRef TX0{a.X[0], 1, (long long)Z * d, d};
