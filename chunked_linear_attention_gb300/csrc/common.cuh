@@ -334,6 +334,55 @@ __device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t cta_mask)
       : "memory");
 }
 
+// Warp-issued forms.  A tensor-core issue loop runs on all 32 lanes of its
+// warp, so that the descriptors and loop state it computes are warp-uniform;
+// one lane, picked by elect.sync inside the instruction sequence, issues each
+// tcgen05 operation.  The same loop run by a single lane inside a divergent
+// branch issues far below the tensor-core rate (measured: about 2.3x slower
+// per 128 x 192 x 16 MMA on sm_103a).  Every lane of the warp must execute
+// these calls together.
+__device__ __forceinline__ void umma_bf16_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void umma_commit_w(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_mc_w(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// Bounded waits by a whole warp: every lane polls, and the warp takes one
+// outcome (a time-out seen by any lane is a time-out for all), so the lanes
+// never part before the next warp-issued operation.
+__device__ __forceinline__ bool mbar_wait_w(uint64_t* bar, uint32_t parity, int* status,
+                                            unsigned long long limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, limit_ns));
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster_w(uint64_t* bar, uint32_t parity, int* status,
+                                                    unsigned long long limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait_cluster(bar, parity, status, limit_ns));
+}
+
 // 16 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   uint32_t r[16];

@@ -5,7 +5,8 @@
 // One CTA per SM (the whole 227 KB of shared memory, all 512 TMEM columns)
 // walks the launch's tiles with a static stride of gridDim.x.  Warp roles:
 // lane 0 of warps 0 and 2 issue TMA loads into a ring of stages (alternate
-// entries), warp 1 issues tcgen05.mma from one thread, warps 3.. drain TMEM
+// entries), warp 1 issues tcgen05.mma (the whole warp runs the loop, one
+// elected lane issues), warps 3.. drain TMEM
 // (tcgen05.ld) and run the epilogue.  When a tile needs at most 256 TMEM columns the accumulator is
 // double-buffered, so the epilogue of one tile overlaps the MMAs of the next;
 // the producer always runs ahead into the next tile.  Every wait is bounded
@@ -116,7 +117,7 @@ __global__ void __launch_bounds__(kGemmKernelThreads, 1)
       if (plane == 0) drain_producer(full, nstages, s, ph, filled, L.status, lim);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    {   // the whole warp walks the loop; one elected lane issues
       int s = 0, it = 0;
       uint32_t ph = 0;
       const uint32_t tiles_saddr = smem_u32(tiles);
@@ -126,11 +127,11 @@ __global__ void __launch_bounds__(kGemmKernelThreads, 1)
         const SmemPlan& sp = plans[tc.prob];
         const int buf = it % nbuf;
         const uint32_t bph = (it / nbuf) & 1;
-        if (!mbar_wait(&acce[buf], bph ^ 1, L.status, lim)) break;
+        if (!mbar_wait_w(&acce[buf], bph ^ 1, L.status, lim)) break;
         tc_fence_after();
         const bool ok = mma_tile(P, sp, tiles_saddr, stage_bytes, nstages, full, empty,
                                  tmem + buf * 256, s, ph, L.status, lim);
-        umma_commit(&accf[buf]);
+        umma_commit_w(&accf[buf]);
         if (!ok) break;
       }
       // the main loops are done: the next launch may start its setup while the

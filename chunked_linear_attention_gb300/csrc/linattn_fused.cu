@@ -24,8 +24,8 @@
 // the reads; bounded waits).  Since every item an item waits for has a
 // smaller index and every CTA walks its items in order, the waits end.
 //
-// Warp roles (192 threads): warp 0 lane 0 issues TMA loads, warp 1 lane 0 the
-// MMAs, warps 2..5 scale, drain TMEM (warp w reads lanes 32 (w % 4) ..) and
+// Warp roles (192 threads): warp 0 lane 0 issues TMA loads, warp 1 the MMAs
+// (one elected lane issues), warps 2..5 scale, drain TMEM (warp w reads lanes 32 (w % 4) ..) and
 // run the prefix items.  Every mbarrier and counter wait is bounded and
 // reports TTT_ERR_TIMEOUT.
 #include <atomic>
@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    {   // the whole warp walks the items; one elected lane issues
       int s = 0, u = 0, nb = 0;
       uint32_t ph = 0;
       bool ok = true;
@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
         if (it.kind == 0) {
           if (!chunk_updates(L, it.c)) continue;
           const int buf = u & 1;
-          if (!mbar_wait(&acce[buf], ((u >> 1) & 1) ^ 1, L.status, lim)) { ok = false; break; }
+          if (!mbar_wait_w(&acce[buf], ((u >> 1) & 1) ^ 1, L.status, lim)) { ok = false; break; }
           tc_fence_after();
           // A = V~^T (M = d_v, K = tokens), B = K^T (N = d_k): both MN-major,
           // 64-column blocks of 128 token rows 16 KB apart
@@ -366,19 +366,19 @@ __global__ void __launch_bounds__(kLThreads, 1)
             // scaled[s] completes once per A-stage use of slot s; a CTA's A
             // items all come before its B items, so its A stages fill the first
             // ring rounds and the ring phase is the barrier's phase
-            if (!mbar_wait(&scaled[s], ph, L.status, lim)) { ok = false; break; }
+            if (!mbar_wait_w(&scaled[s], ph, L.status, lim)) { ok = false; break; }
             tc_fence_after();
             const uint64_t so = (uint64_t)(s * stage16);
 #pragma unroll
             for (int kk = 0; kk < kLTok / 16; ++kk)   // 16 token rows = 2 KB
-              umma_bf16(d, a0 + so + kk * 128, b0 + so + kk * 128, idesc, (j | kk) != 0);
-            umma_commit(&empty[s]);
+              umma_bf16_w(d, a0 + so + kk * 128, b0 + so + kk * 128, idesc, (j | kk) != 0);
+            umma_commit_w(&empty[s]);
             ring_next(s, ph, nstages);
           }
-          umma_commit(&accf[buf]);
+          umma_commit_w(&accf[buf]);
           ++u;
         } else if (it.kind == 2) {
-          if (!mbar_wait(sfull, nb & 1, L.status, lim)) { ok = false; break; }
+          if (!mbar_wait_w(sfull, nb & 1, L.status, lim)) { ok = false; break; }
           ++nb;
           // A = Q rows (K-major, K = d_k), B = S (K-major: N = d_v rows, K = d_k)
           const uint32_t idesc = idesc_bf16_f32(L.dv, 0, 0);
@@ -386,23 +386,23 @@ __global__ void __launch_bounds__(kLThreads, 1)
           const uint64_t b0 = smem_desc_sw128(s_saddr, 16, 1024);
           for (int mt = 0; mt < L.rb / kLTok && ok; ++mt) {
             const int buf = u & 1;
-            if (!mbar_wait(&acce[buf], ((u >> 1) & 1) ^ 1, L.status, lim)) { ok = false; break; }
-            if (!mbar_wait(&full[s], ph, L.status, lim)) { ok = false; break; }
+            if (!mbar_wait_w(&acce[buf], ((u >> 1) & 1) ^ 1, L.status, lim)) { ok = false; break; }
+            if (!mbar_wait_w(&full[s], ph, L.status, lim)) { ok = false; break; }
             tc_fence_after();
             const uint64_t so = (uint64_t)(s * stage16);
             const uint32_t d = tmem + buf * 128;
             for (int b = 0; b < dkb; ++b) {   // 64 of K per block: A 16 KB, S d_v x 128 B apart
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                umma_bf16(d, a0 + so + b * 1024 + kk * 2, b0 + b * (L.dv * 8) + kk * 2, idesc,
+                umma_bf16_w(d, a0 + so + b * 1024 + kk * 2, b0 + b * (L.dv * 8) + kk * 2, idesc,
                           (b | kk) != 0);
             }
-            umma_commit(&empty[s]);
-            umma_commit(&accf[buf]);
+            umma_commit_w(&empty[s]);
+            umma_commit_w(&accf[buf]);
             ring_next(s, ph, nstages);
             ++u;
           }
-          umma_commit(sempty);
+          umma_commit_w(sempty);
         }
       }
     }

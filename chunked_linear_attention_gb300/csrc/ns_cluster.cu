@@ -157,20 +157,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       } else if (warp == 1) {
-        if (lane == 0 && ok) {
+        if (ok) {   // the whole warp walks the loop; one elected lane issues
           SmemPlan sp;
           plan_problem(P, sp);
           for (int tile = rank; tile < ntiles; tile += L.cs, ++it_mma) {
             const int buf = it_mma & 1;
             const uint32_t bph = (it_mma >> 1) & 1;
-            if (!mbar_wait(&acce[buf], bph ^ 1, L.status, lim)) {
+            if (!mbar_wait_w(&acce[buf], bph ^ 1, L.status, lim)) {
               ok = false;
               break;
             }
             tc_fence_after();
             const bool good = mma_tile(P, sp, tiles_saddr, stage_bytes, nstages, full, empty,
                                        tmem + buf * 256, s_mma, ph_mma, L.status, lim);
-            umma_commit(&accf[buf]);
+            umma_commit_w(&accf[buf]);
             if (!good) {
               ok = false;
               break;

@@ -14,9 +14,10 @@
 // partner (r, 1-h), completing on the partner's panel barrier.  The B operand
 // is column half h of the previous product (rows of X or G for the Gram and
 // polynomial products, X as MN-major for the step); it streams from L2
-// through a ring of 64-deep K slices, each slice fetched in 64-row shares by
-// the R CTAs of the same half and multicast to all of them.  Every CTA thus
-// reads half of B per product (the work per CTA is half a row panel).  G and
+// through a ring of 64-deep K slices that every CTA fetches for itself (a
+// slice multicast to the R CTAs of the half measured slower: a stage could
+// only be refilled once all of them had consumed it).  Every CTA thus reads
+// half of B per product (the work per CTA is half a row panel).  G and
 // X' also go to global memory by TMA store for the next products' B
 // operands, followed by a cluster barrier (two per step; P stays in shared
 // memory).  The MMA commits of a product arrive at both partners, so neither
@@ -27,7 +28,7 @@
 // waits for the partner's half only before the rest.
 //
 // Warp roles (320 threads): warp 0 lane 0 issues the TMA loads, warp 1
-// lane 0 the tcgen05 MMAs (M = 128, N = d/2), warps 2..9 drain TMEM (warp w
+// the tcgen05 MMAs (M = 128, N = d/2; one elected lane issues), warps 2..9 drain TMEM (warp w
 // reads lanes 32 (w % 4) .., column quarter (w - 2) / 4 of the half).  Every
 // mbarrier wait is bounded and reports TTT_ERR_TIMEOUT; every thread reaches
 // every cluster barrier.
@@ -250,7 +251,6 @@ __global__ void __launch_bounds__(kHThreads, 1)
   const int rank = (int)cluster_ctarank();
   const int h = rank / R, r = rank % R;        // column half, row panel
   const int partner = (1 - h) * R + r;
-  const uint16_t hmask = (uint16_t)(((1u << R) - 1u) << (h * R));   // CTAs of this half
   const uint16_t pmask = (uint16_t)((1u << rank) | (1u << partner));
   const int zl = blockIdx.x / (2 * R);
   const int z = (L.slot0 + zl / L.nh) * L.BH + L.h0 + (zl % L.nh);
@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(kHThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < nstages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], R);
+      mbar_init(&empty[s], 1);
     }
     mbar_init(mma_done, 2);
     mbar_init(own_ready, 1);
@@ -330,17 +330,17 @@ __global__ void __launch_bounds__(kHThreads, 1)
               }
               mbar_arrive_expect_tx(&full[s_prod], stage_bytes);
               uint8_t* dst = ring + s_prod * stage_bytes;
-              // one box per K slice, issued in turn by the CTAs of the half and
-              // multicast to all of them
-              const bool mine = i % R == r;
+              // the whole K slice of this CTA's column half (one box, or R shares)
               if (kind == 2) {   // X as MN-major B: K = rows of X, N = its columns of half h
-                if (L.mn_split)
-                  tma_load_2d_mc(dst + r * 8192, map, h * half + r * 64, mrow + ks * 64,
-                                 &full[s_prod], hmask);
-                else if (mine)
-                  tma_load_3d_mc(dst, map, 0, mrow + ks * 64, h * R, &full[s_prod], hmask);
-              } else if (mine) {   // rows of X or G of half h as K-major B
-                tma_load_2d_mc(dst, map, ks * 64, mrow + h * half, &full[s_prod], hmask);
+                if (L.mn_split) {
+                  for (int j = 0; j < R; ++j)
+                    tma_load_2d(dst + j * 8192, map, h * half + j * 64, mrow + ks * 64,
+                                &full[s_prod]);
+                } else {
+                  tma_load_3d(dst, map, 0, mrow + ks * 64, h * R, &full[s_prod]);
+                }
+              } else {   // rows of X or G of half h as K-major B
+                tma_load_2d(dst, map, ks * 64, mrow + h * half, &full[s_prod]);
               }
             }
             ++issued;   // every producer lane walks every entry
@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(kHThreads, 1)
         }
       }
     } else if (warp == 1) {
-      if (lane == 0 && ok) {
+      if (ok) {   // the whole warp walks the loop; one elected lane issues
         // descriptors advanced by byte offset / 16 in the start-address field
         const uint64_t a_desc0 = smem_desc_sw128(smem_u32(apanel), 16, 1024);
         const uint64_t bk_desc0 = smem_desc_sw128(smem_u32(ring), 16, 1024);     // K-major B
@@ -363,8 +363,8 @@ __global__ void __launch_bounds__(kHThreads, 1)
           // The K slices of this CTA's own half of the A panel come first (its
           // own epilogue wrote them); the partner's half is waited for only
           // before the remaining slices, so the exchange hides behind them.
-          ok = p == 0 ? mbar_wait(abar, 0, L.status, lim)
-                      : mbar_wait(own_ready, (uint32_t)((p - 1) & 1), L.status, lim);
+          ok = p == 0 ? mbar_wait_w(abar, 0, L.status, lim)
+                      : mbar_wait_w(own_ready, (uint32_t)((p - 1) & 1), L.status, lim);
           if (!ok) break;
           tc_fence_after();
           const uint32_t idesc = idesc_bf16_f32(half, 0, kind == 2 ? 1 : 0);
@@ -373,30 +373,30 @@ __global__ void __launch_bounds__(kHThreads, 1)
           for (int i = 0; i < nk; ++i) {
             const int ks = i < R ? h * R + i : (1 - h) * R + i - R;
             if (i == R && p > 0) {
-              if (!mbar_wait_cluster(pready, (uint32_t)((p - 1) & 1), L.status, lim)) {
+              if (!mbar_wait_cluster_w(pready, (uint32_t)((p - 1) & 1), L.status, lim)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
             }
-            if (!mbar_wait(&full[s_mma], ph_mma, L.status, lim)) {
+            if (!mbar_wait_w(&full[s_mma], ph_mma, L.status, lim)) {
               ok = false;
               break;
             }
             tc_fence_after();
             const uint64_t ad = a_desc0 + (uint64_t)(ks * (kHChunk / 16));
             const uint64_t bd = b_desc0 + (uint64_t)(s_mma * stage16);
-            umma_bf16(tmem, ad, bd, idesc, i != 0);
-            umma_bf16(tmem, ad + 2, bd + bkk, idesc, 1);
-            umma_bf16(tmem, ad + 4, bd + 2 * bkk, idesc, 1);
-            umma_bf16(tmem, ad + 6, bd + 3 * bkk, idesc, 1);
-            umma_commit_mc(&empty[s_mma], hmask);
+            umma_bf16_w(tmem, ad, bd, idesc, i != 0);
+            umma_bf16_w(tmem, ad + 2, bd + bkk, idesc, 1);
+            umma_bf16_w(tmem, ad + 4, bd + 2 * bkk, idesc, 1);
+            umma_bf16_w(tmem, ad + 6, bd + 3 * bkk, idesc, 1);
+            umma_commit_w(&empty[s_mma]);
             if (++s_mma == nstages) {
               s_mma = 0;
               ph_mma ^= 1;
             }
           }
-          if (ok) umma_commit_mc(mma_done, pmask);   // this product done, at both partners
+          if (ok) umma_commit_mc_w(mma_done, pmask);   // this product done, at both partners
         }
       }
     } else {
@@ -475,7 +475,7 @@ __global__ void __launch_bounds__(kHThreads, 1)
   // while the update finishes
   if (warp == 1 && lane == 0) pdl_launch_dependents();
 
-  // every peer's multicast commit into our ring barriers must have landed
+  // the last commits into our ring barriers must have landed before the exit
   if (warp == 0 && lane == 0 && ok) {
     const int n = issued < nstages ? issued : nstages;
     for (int i = 0; i < n; ++i) {

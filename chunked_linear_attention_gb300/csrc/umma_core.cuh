@@ -232,7 +232,8 @@ __device__ __forceinline__ void drain_producer(uint64_t* full, int nstages, int 
   }
 }
 
-// MMA issuer (one thread): accumulates one tile into TMEM at column tmem_acc
+// MMA issue loop, run by a whole warp (one elected lane issues each
+// tcgen05 operation): accumulates one tile into TMEM at column tmem_acc
 // (accumulator j at tmem_acc + j * bn).  Descriptors are scalars built once
 // per group; no runtime-indexed arrays in the k-step loop.
 static __device__ __forceinline__ bool mma_tile(const Problem& P, const SmemPlan& sp,
@@ -273,7 +274,7 @@ static __device__ __forceinline__ bool mma_tile(const Problem& P, const SmemPlan
     const uint32_t ha = a_mn ? 512 : kBM * 8, hb0 = bmn0 ? 512 : P.bn * 8;   // next 64 of K
     const uint32_t stage16 = stage_bytes >> 4;
     for (int ks = 0; ks < nk; ++ks) {
-      if (!mbar_wait(&full[s], ph, status, lim)) return false;
+      if (!mbar_wait_w(&full[s], ph, status, lim)) return false;
       tc_fence_after();
       const uint64_t so = (uint64_t)(s * stage16);
       for (int kh = 0; kh < kd; ++kh) {
@@ -282,12 +283,12 @@ static __device__ __forceinline__ bool mma_tile(const Problem& P, const SmemPlan
         for (int kk = 0; kk < kBK / 16; ++kk) {
           const uint32_t acc = (ks | kh | kk) != 0;
           const uint64_t ad = ah + kk * ka;
-          umma_bf16(d0, ad, bh + kk * kb0, id0, acc);
-          if (nmma > 1) umma_bf16(d1, ad, b1 + so + kk * kb1, id1, acc);
-          if (nmma > 2) umma_bf16(d2, ad, b2 + so + kk * kb2, id2, acc);
+          umma_bf16_w(d0, ad, bh + kk * kb0, id0, acc);
+          if (nmma > 1) umma_bf16_w(d1, ad, b1 + so + kk * kb1, id1, acc);
+          if (nmma > 2) umma_bf16_w(d2, ad, b2 + so + kk * kb2, id2, acc);
         }
       }
-      umma_commit(&empty[s]);
+      umma_commit_w(&empty[s]);
       if (++s == nstages) {
         s = 0;
         ph ^= 1;
