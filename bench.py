@@ -404,38 +404,72 @@ def time_extra_workload(torch, cla, wl, dev, stream, peaks, steps, warmup):
 
 
 def time_linattn(torch, cla, dev, stream, peaks):
-    """The chunked linear-attention workload (HBM-bound): L2 flushed before
-    every call, CUDA-event time of the call alone."""
+    """The chunked linear-attention workload (HBM-bound), CUDA-event time per
+    call.  Main figure: calls back to back over three independently drawn
+    input sets whose I/O together (3 x 134.7 MB) is three times L2, so every
+    call reads its inputs from HBM.  Beside it: the call alone after a 256 MB
+    write flush, whose dirty lines are written back during the call."""
     import workloads
     lw = workloads.LINATTN_C2
-    lq, lk, lv, leta, _ = [t.to(dev) if t is not None else None
-                           for t in workloads.linattn_inputs(lw)]
-    lo = torch.empty_like(lq)
-    lS = torch.empty((lw.B, lw.H, lw.d_v, lw.d_k), device=dev)
+    nsets = 3
+    sets = []
+    for j in range(nsets):
+        lq, lk, lv, leta, _ = [t.to(dev) if t is not None else None
+                               for t in workloads.linattn_inputs(lw, seed=lw.seed + j)]
+        sets.append((lq, lk, lv, leta, torch.empty_like(lq),
+                     torch.empty((lw.B, lw.H, lw.d_v, lw.d_k), device=dev)))
     lws = torch.empty(cla.linattn_workspace_size(lw.B, lw.H, lw.N, lw.d_k, lw.d_v, lw.chunk,
                                                  cla.TTT_BF16, lw.mode),
                       device=dev, dtype=torch.uint8)
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    tot, reps = 0.0, 20
-    for i in range(reps + 3):
-        flush.zero_()    # evict the inputs from L2 between repetitions
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        cla.linattn_chunked_forward(lq, lk, lv, leta, lw.chunk, lw.mode, out=lo, S_final=lS,
+
+    def call(j):
+        q_, k_, v_, eta_, o_, S_ = sets[j % nsets]
+        cla.linattn_chunked_forward(q_, k_, v_, eta_, lw.chunk, lw.mode, out=o_, S_final=S_,
                                     workspace=lws)
-        e1.record(stream)
+
+    for j in range(3 * nsets):
+        call(j)
+    torch.cuda.synchronize()
+    check_status(cla)
+    reps = 10 * nsets
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    h0 = time.perf_counter()
+    e0.record(stream)
+    for j in range(reps):
+        call(j)
+    e1.record(stream)
+    host_us = (time.perf_counter() - h0) * 1e6 / reps
+    torch.cuda.synchronize()
+    lms = e0.elapsed_time(e1) / reps
+
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    tot, nf = 0.0, 10
+    for i in range(nf + 3):
+        flush.zero_()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        call(0)
+        f1.record(stream)
         torch.cuda.synchronize()
         if i >= 3:
-            tot += e0.elapsed_time(e1)
+            tot += f0.elapsed_time(f1)
     check_status(cla)
-    lms = tot / reps
+    fms = tot / nf
+    lq, leta, lo = sets[0][0], sets[0][3], sets[0][4]
     io_bytes = (3 * lq.numel() * 2 + leta.numel() * 4 + lo.numel() * 2)
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     return {"workload": lw.name, "us_per_call": lms * 1e3,
             "tokens_per_s": lw.B * lw.N / (lms / 1e3),
             "gbs": io_bytes / (lms / 1e3) / 1e9, "hbm_frac": io_bytes / (lms / 1e3) / 1e9 / hbm,
-            "io_bytes": io_bytes, "l2": "flushed (256 MB write) before each call"}
+            "io_bytes": io_bytes, "host_enqueue_us_per_call": host_us,
+            "l2": "inputs larger than L2: calls back to back over %d input sets (%.0f MB of I/O)"
+                  % (nsets, nsets * io_bytes / 1e6),
+            "after_write_flush": {"us_per_call": fms * 1e3,
+                                  "gbs": io_bytes / (fms / 1e3) / 1e9,
+                                  "note": "one call after a 256 MB write to L2; the flush's "
+                                          "dirty lines are written back during the call"}}
 
 
 def time_variants(torch, cla, dev, stream, steps=10, warmup=3):

@@ -140,12 +140,13 @@ __device__ __forceinline__ void ring_next(int& s, uint32_t& ph, int nstages) {
   }
 }
 
-// One prefix item: elements [e0, e1) of batch-head bh's state.  Thread t
-// owns the element groups (4 elements) e0 + 4 t + 512 g, g < kPG, and carries
-// their running states across the chunks; the partials of kPB (chunk, split)
-// pairs for all of its groups are loaded before any is added, so those
-// kPG x kPB loads are in flight together.
-constexpr int kPB = 8;
+// One prefix item: the `per` (<= 2048) elements from e0 of batch-head bh's
+// state.  Thread t owns the element groups (4 elements) e0 + 4 t + 512 g,
+// g < kPG, and carries their running states across the chunks.  The
+// producer warp brings the item's (chunk, split) partial slices into the
+// ring by bulk copies, as many per stage as fit (generic loads of those
+// partials measured slow: they finished ~9.5 us after the last A item,
+// wherever they were issued).
 constexpr int kPG = 4;
 
 __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* r, float4 v) {
@@ -161,85 +162,87 @@ __device__ __forceinline__ void fma4(float4& y, float a, const float4& x) {
 }
 
 // Per updating chunk c: M <- alpha_c M + G_c, S <- S + lr_c M (rule.mom), or
-// S <- S + lr_c G_c; chunks that do not update leave both unchanged.
-__device__ __forceinline__ void prefix_item(const LinFusedLaunch& L, int bh, int e0, int e1,
-                                            int tid) {
+// S <- S + lr_c G_c; chunks that do not update leave both unchanged.  Run by
+// the four epilogue warps together (tid 0..127); walks the item's ring stages
+// in step with the producer (s, ph) and releases each one.
+__device__ __forceinline__ void prefix_item(const LinFusedLaunch& L, int bh, int e0, int per,
+                                            int tid, const uint8_t* ring, uint64_t* full,
+                                            uint64_t* empty, int& s, uint32_t& ph, bool& ok) {
   const long long E = (long long)L.dv * L.dk;
   const int npairs = L.nc * L.splits;
+  const uint32_t sl = (uint32_t)per * 4;
+  const int pps = (int)(L.stage_bytes / sl);
   const LinRule& R = L.rule;
-  for (int eb = e0; eb < e1; eb += 4 * 128 * kPG) {
-    float4 s[kPG], add[kPG], m[kPG];
-    bool own[kPG];
+  float4 s4[kPG], add[kPG], m[kPG];
+  bool own[kPG];
 #pragma unroll
-    for (int g = 0; g < kPG; ++g) {
-      const int e = eb + 4 * tid + 512 * g;
-      own[g] = e < e1;
-      s[g] = (own[g] && L.S0) ? *reinterpret_cast<const float4*>(L.S0 + bh * E + e)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-      m[g] = (own[g] && R.M0) ? *reinterpret_cast<const float4*>(R.M0 + bh * E + e)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-      add[g] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    const float* pbase = L.partials + (long long)bh * npairs * E + eb + 4 * tid;
-    for (int p0 = 0; p0 < npairs; p0 += kPB) {
-      float4 v[kPB][kPG];
-#pragma unroll
-      for (int j = 0; j < kPB; ++j) {
-        const int pr = p0 + j;
-        const bool live = pr < npairs && chunk_updates(L, pr / L.splits);
-#pragma unroll
-        for (int g = 0; g < kPG; ++g)
-          v[j][g] = (live && own[g])
-                        ? *reinterpret_cast<const float4*>(pbase + (long long)pr * E + 512 * g)
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int j = 0; j < kPB; ++j) {
-        const int pr = p0 + j;
-        if (pr >= npairs) break;
-#pragma unroll
-        for (int g = 0; g < kPG; ++g) {
-          add[g].x += v[j][g].x; add[g].y += v[j][g].y;
-          add[g].z += v[j][g].z; add[g].w += v[j][g].w;
-        }
-        if ((pr + 1) % L.splits != 0) continue;
-        // chunk pr / splits complete: the state it reads, then the running state
-        const int c = pr / L.splits;
-        const bool upd = chunk_updates(L, c);
-        const float lr = (upd && R.lr) ? R.lr[(long long)bh * L.nc + c] : R.lr_const;
-        const float al = (upd && R.mom && R.alpha) ? R.alpha[(long long)bh * L.nc + c]
-                                                   : R.alpha_const;
+  for (int g = 0; g < kPG; ++g) {
+    const int off = 4 * tid + 512 * g;
+    own[g] = off < per;
+    s4[g] = (own[g] && L.S0) ? *reinterpret_cast<const float4*>(L.S0 + bh * E + e0 + off)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+    m[g] = (own[g] && R.M0) ? *reinterpret_cast<const float4*>(R.M0 + bh * E + e0 + off)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    add[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int p0 = 0; p0 < npairs; p0 += pps) {
+    if (ok) ok = mbar_wait(&full[s], ph, L.status, L.wait_limit_ns);
+    ok = __all_sync(0xffffffffu, ok);
+    const uint32_t st = smem_u32(ring + s * L.stage_bytes) + (uint32_t)tid * 16u;
+    for (int j = 0; j < pps; ++j) {
+      const int pr = p0 + j;
+      if (pr >= npairs) break;
+      if (ok && chunk_updates(L, pr / L.splits)) {
 #pragma unroll
         for (int g = 0; g < kPG; ++g) {
           if (!own[g]) continue;
-          float4 inc = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (upd) {
-            if (R.mom) {
-              float4 mm = add[g];
-              fma4(mm, al, m[g]);
-              m[g] = mm;
-              fma4(inc, lr, mm);
-            } else {
-              fma4(inc, lr, add[g]);
-            }
-          }
-          float4 rd = s[g];
-          if (!L.apply_first) {
-            rd.x += inc.x; rd.y += inc.y; rd.z += inc.z; rd.w += inc.w;
-          }
-          store_bf16x4(L.s_read + (long long)(bh * L.nc + c) * E + eb + 4 * tid + 512 * g, rd);
-          s[g].x += inc.x; s[g].y += inc.y; s[g].z += inc.z; s[g].w += inc.w;
-          add[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+          const uint4 w = lds128(st + (uint32_t)j * sl + 2048u * g);
+          add[g].x += __uint_as_float(w.x); add[g].y += __uint_as_float(w.y);
+          add[g].z += __uint_as_float(w.z); add[g].w += __uint_as_float(w.w);
         }
       }
-    }
+      if ((pr + 1) % L.splits != 0) continue;
+      // chunk pr / splits complete: the state it reads, then the running state
+      const int c = pr / L.splits;
+      const bool upd = chunk_updates(L, c);
+      const float lr = (upd && R.lr) ? R.lr[(long long)bh * L.nc + c] : R.lr_const;
+      const float al = (upd && R.mom && R.alpha) ? R.alpha[(long long)bh * L.nc + c]
+                                                 : R.alpha_const;
 #pragma unroll
-    for (int g = 0; g < kPG; ++g) {
-      if (!own[g]) continue;
-      const long long o = bh * E + eb + 4 * tid + 512 * g;
-      if (L.s_final) *reinterpret_cast<float4*>(L.s_final + o) = s[g];
-      if (R.M_final) *reinterpret_cast<float4*>(R.M_final + o) = m[g];
+      for (int g = 0; g < kPG; ++g) {
+        if (!own[g]) continue;
+        float4 inc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (upd) {
+          if (R.mom) {
+            float4 mm = add[g];
+            fma4(mm, al, m[g]);
+            m[g] = mm;
+            fma4(inc, lr, mm);
+          } else {
+            fma4(inc, lr, add[g]);
+          }
+        }
+        float4 rd = s4[g];
+        if (!L.apply_first) {
+          rd.x += inc.x; rd.y += inc.y; rd.z += inc.z; rd.w += inc.w;
+        }
+        if (ok)
+          store_bf16x4(L.s_read + (long long)(bh * L.nc + c) * E + e0 + 4 * tid + 512 * g, rd);
+        s4[g].x += inc.x; s4[g].y += inc.y; s4[g].z += inc.z; s4[g].w += inc.w;
+        add[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
+    named_bar_sync(1, 128);   // every thread is done with the stage
+    if (tid == 0 && ok) mbar_arrive(&empty[s]);
+    ring_next(s, ph, L.nstages);
+  }
+  if (!ok) return;
+#pragma unroll
+  for (int g = 0; g < kPG; ++g) {
+    if (!own[g]) continue;
+    const long long o = bh * E + e0 + 4 * tid + 512 * g;
+    if (L.s_final) *reinterpret_cast<float4*>(L.s_final + o) = s4[g];
+    if (R.M_final) *reinterpret_cast<float4*>(R.M_final + o) = m[g];
   }
 }
 
@@ -318,6 +321,28 @@ __global__ void __launch_bounds__(kLThreads, 1)
                           &full[s]);
             ring_next(s, ph, nstages);
           }
+        } else if (it.kind == 1) {
+          // the batch-head's partial slices for this item, through the ring;
+          // chunks that do not update wrote none and are skipped
+          if (!wait_count(doneA + it.bh, L.n_upd * L.splits, L.status, lim)) { ok = false; break; }
+          fence_proxy_async_global();
+          const int E = L.dv * L.dk, per = E / L.pparts, npairs = L.nc * L.splits;
+          const uint32_t sl = (uint32_t)per * 4;
+          const int pps = (int)(stage_bytes / sl);
+          const float* base = L.partials + (long long)it.bh * npairs * E + (long long)it.sub * per;
+          for (int p0 = 0; p0 < npairs && ok; p0 += pps) {
+            if (!mbar_wait(&empty[s], ph ^ 1, L.status, lim)) { ok = false; break; }
+            const int n = min(pps, npairs - p0);
+            uint32_t bytes = 0;
+            for (int j = 0; j < n; ++j)
+              if (chunk_updates(L, (p0 + j) / L.splits)) bytes += sl;
+            mbar_arrive_expect_tx(&full[s], bytes);
+            uint8_t* st = ring + s * stage_bytes;
+            for (int j = 0; j < n; ++j)
+              if (chunk_updates(L, (p0 + j) / L.splits))
+                bulk_load_g2s(st + j * sl, base + (long long)(p0 + j) * E, sl, &full[s]);
+            ring_next(s, ph, nstages);
+          }
         } else if (it.kind == 2) {
           const int qrow0 = it.bh * L.N + it.c * L.chunk + it.sub * L.rb;
           prefetch_rows_l2(L.q + (long long)qrow0 * L.dk, (uint32_t)L.rb * L.dk * 2);
@@ -377,6 +402,10 @@ __global__ void __launch_bounds__(kLThreads, 1)
           }
           umma_commit_w(&accf[buf]);
           ++u;
+        } else if (it.kind == 1) {   // the prefix warps consume these stages
+          const int per = L.dv * L.dk / L.pparts;
+          const int pps = (int)(stage_bytes / ((uint32_t)per * 4));
+          for (int p0 = 0; p0 < L.nc * L.splits; p0 += pps) ring_next(s, ph, nstages);
         } else if (it.kind == 2) {
           if (!mbar_wait_w(sfull, nb & 1, L.status, lim)) { ok = false; break; }
           ++nb;
@@ -498,15 +527,8 @@ __global__ void __launch_bounds__(kLThreads, 1)
           atomicAdd(doneA + it.bh, 1);
         }
       } else if (it.kind == 1) {
-        bool got = true;
-        if (lane == 0 && ok)
-          got = wait_count(doneA + it.bh, L.n_upd * L.splits, L.status, lim);
-        ok = ok && __shfl_sync(0xffffffffu, got, 0);
-        named_bar_sync(1, 128);
-        if (ok) {
-          const int E = L.dv * L.dk, per = E / L.pparts;
-          prefix_item(L, it.bh, it.sub * per, (it.sub + 1) * per, tid);
-        }
+        const int per = L.dv * L.dk / L.pparts;
+        prefix_item(L, it.bh, it.sub * per, per, tid, ring, full, empty, s, ph, ok);
         named_bar_sync(1, 128);
         if (tid == 0 && ok) {
           __threadfence();
@@ -568,6 +590,9 @@ bool linattn_fused_applicable(const LinDims& D) {
   if ((D.dk != 64 && D.dk != 128) || D.dv != 128) return false;
   if (D.chunk % kLTok != 0 || D.N % D.chunk != 0) return false;
   if (D.N / D.chunk > kMaxFlagChunks) return false;
+  // a prefix item's slice of the state (d_v d_k / 8 elements, eight items per
+  // batch-head) is one pass of its 128 threads
+  if (D.dv * D.dk / 8 > 4 * 128 * kPG) return false;
   return true;
 }
 
