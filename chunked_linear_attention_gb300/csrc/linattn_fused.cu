@@ -69,6 +69,8 @@ struct LinFusedLaunch {
   int* status;
   unsigned long long wait_limit_ns;
   int withhold_bh;            // test hook: this batch-head's A items never release (-1: none)
+  int blocked;                // maps are 3-D blocked views: one box per tile (all 64-column
+                              // blocks), else 2-D maps and one box per 64-column block
 };
 
 static_assert(sizeof(LinFusedLaunch) <= 4096, "kernel parameter block too large");
@@ -314,11 +316,16 @@ __global__ void __launch_bounds__(kLThreads, 1)
             if (!mbar_wait(&empty[s], ph ^ 1, L.status, lim)) { ok = false; break; }
             mbar_arrive_expect_tx(&full[s], (uint32_t)(L.dv + L.dk) * kLTok * 2);
             uint8_t* st = ring + s * stage_bytes;
-            for (int b = 0; b < dvb; ++b)
-              tma_load_2d(st + b * 16384, &L.maps[LM_V], b * 64, row0 + j * kLTok, &full[s]);
-            for (int b = 0; b < dkb; ++b)
-              tma_load_2d(st + (dvb + b) * 16384, &L.maps[LM_K], b * 64, row0 + j * kLTok,
-                          &full[s]);
+            if (L.blocked) {
+              tma_load_3d(st, &L.maps[LM_V], 0, row0 + j * kLTok, 0, &full[s]);
+              tma_load_3d(st + dvb * 16384, &L.maps[LM_K], 0, row0 + j * kLTok, 0, &full[s]);
+            } else {
+              for (int b = 0; b < dvb; ++b)
+                tma_load_2d(st + b * 16384, &L.maps[LM_V], b * 64, row0 + j * kLTok, &full[s]);
+              for (int b = 0; b < dkb; ++b)
+                tma_load_2d(st + (dvb + b) * 16384, &L.maps[LM_K], b * 64, row0 + j * kLTok,
+                            &full[s]);
+            }
             ring_next(s, ph, nstages);
           }
         } else if (it.kind == 1) {
@@ -351,17 +358,23 @@ __global__ void __launch_bounds__(kLThreads, 1)
           fence_proxy_async_global();
           if (!mbar_wait(sempty, (nb & 1) ^ 1, L.status, lim)) { ok = false; break; }
           mbar_arrive_expect_tx(sfull, s_bytes);
-          for (int b = 0; b < dkb; ++b)
-            tma_load_2d(sreg + b * L.dv * 128, &L.maps[LM_S], b * 64, (it.bh * L.nc + it.c) * L.dv,
-                        sfull);
+          if (L.blocked)
+            tma_load_3d(sreg, &L.maps[LM_S], 0, (it.bh * L.nc + it.c) * L.dv, 0, sfull);
+          else
+            for (int b = 0; b < dkb; ++b)
+              tma_load_2d(sreg + b * L.dv * 128, &L.maps[LM_S], b * 64,
+                          (it.bh * L.nc + it.c) * L.dv, sfull);
           ++nb;
           const int row0 = it.bh * L.N + it.c * L.chunk + it.sub * L.rb;
           for (int mt = 0; mt < L.rb / kLTok && ok; ++mt) {
             if (!mbar_wait(&empty[s], ph ^ 1, L.status, lim)) { ok = false; break; }
             mbar_arrive_expect_tx(&full[s], (uint32_t)L.dk * kLTok * 2);
             uint8_t* st = ring + s * stage_bytes;
-            for (int b = 0; b < dkb; ++b)
-              tma_load_2d(st + b * 16384, &L.maps[LM_Q], b * 64, row0 + mt * kLTok, &full[s]);
+            if (L.blocked)
+              tma_load_3d(st, &L.maps[LM_Q], 0, row0 + mt * kLTok, 0, &full[s]);
+            else
+              for (int b = 0; b < dkb; ++b)
+                tma_load_2d(st + b * 16384, &L.maps[LM_Q], b * 64, row0 + mt * kLTok, &full[s]);
             ring_next(s, ph, nstages);
           }
         }
@@ -663,8 +676,14 @@ int launch_linattn_fused(MapCache& cache, const LinFusedArgs& a, int* status,
   const TensorRef TK{a.k, 1, (long long)BH * D.N, D.dk};
   const TensorRef TQ{a.q, 1, (long long)BH * D.N, D.dk};
   const TensorRef TS{L.s_read, 1, (long long)BH * nc * D.dv, D.dk};
-  if (!cache.get(TV, kLTok, &L.maps[LM_V]) || !cache.get(TK, kLTok, &L.maps[LM_K]) ||
-      !cache.get(TQ, kLTok, &L.maps[LM_Q]) || !cache.get(TS, D.dv, &L.maps[LM_S]))
+  // one box per tile where the driver takes the blocked view, else one per 64 columns
+  L.blocked = cache.get_blocked(TV, kLTok, D.dv / 64, &L.maps[LM_V]) &&
+              cache.get_blocked(TK, kLTok, D.dk / 64, &L.maps[LM_K]) &&
+              cache.get_blocked(TQ, kLTok, D.dk / 64, &L.maps[LM_Q]) &&
+              cache.get_blocked(TS, D.dv, D.dk / 64, &L.maps[LM_S]);
+  if (!L.blocked &&
+      (!cache.get(TV, kLTok, &L.maps[LM_V]) || !cache.get(TK, kLTok, &L.maps[LM_K]) ||
+       !cache.get(TQ, kLTok, &L.maps[LM_Q]) || !cache.get(TS, D.dv, &L.maps[LM_S])))
     return -4;
   L.eta = a.eta;
   L.S0 = a.S0;
