@@ -434,6 +434,9 @@ def time_linattn(torch, cla, dev, stream, peaks):
     reps = 10 * nsets
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    # keep the GPU busy (~1.5 ms) while the host enqueues the calls, so the
+    # timed calls run back to back on the device whatever the host's pace
+    torch.cuda._sleep(3_000_000)
     h0 = time.perf_counter()
     e0.record(stream)
     for j in range(reps):
