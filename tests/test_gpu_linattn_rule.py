@@ -63,6 +63,10 @@ MOM_CASES = [
     dict(mode=W.STRIDED, chunk=128, N=1024, update_chunks=(1, 0, 1, 1, 0, 0, 1, 0)),
     dict(mode=W.BLOCK_CAUSAL, chunk=256, N=768, d_k=64, d_v=192),
     dict(mode=W.STRIDED, chunk=128, N=768, d_k=128, d_v=64, update_chunks=(0, 1, 1, 0, 1, 0)),
+    # 32 chunks: the prefix items' partial slices cross four ring stages
+    dict(mode=W.APPLY_THEN_UPDATE, chunk=256, N=8192),
+    dict(mode=W.STRIDED, chunk=256, N=8192,
+         update_chunks=tuple(int(c % 4 != 3 and c > 1) for c in range(32))),
 ]
 
 

@@ -209,6 +209,11 @@ LIN_CASES = [
     dict(mode=W.STRIDED, chunk=128, N=1024, update_chunks=(0, 1, 1, 0, 1, 0, 0, 1)),
     dict(mode=W.BLOCK_CAUSAL, chunk=256, N=768, d_k=64, d_v=192),
     dict(mode=W.APPLY_THEN_UPDATE, chunk=512, N=2048, d_k=64, d_v=128),
+    # 32 chunks of one-launch shape: each prefix item takes its 32 partial
+    # slices through four ring stages (eight per stage at d_k = d_v = 128)
+    dict(mode=W.BLOCK_CAUSAL, chunk=256, N=8192),
+    dict(mode=W.STRIDED, chunk=256, N=8192,
+         update_chunks=tuple(int(c % 3 != 1 and c < 29) for c in range(32))),
 ]
 
 
