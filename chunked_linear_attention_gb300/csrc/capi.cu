@@ -147,7 +147,7 @@ const char* ttt_status_string(int status) {
     case TTT_ERR_NULL: return "a required pointer is NULL";
     case TTT_ERR_SHAPE: return "inconsistent sizes";
     case TTT_ERR_ALIGN: return "pointer not 16-byte aligned (workspace: 256-byte)";
-    case TTT_ERR_UNSUPPORTED: return "request not supported by this build";
+    case TTT_ERR_UNSUPPORTED: return "request not supported by this library";
     case TTT_ERR_WORKSPACE: return "workspace missing or too small";
     case TTT_ERR_CUDA: return "CUDA runtime error";
     case TTT_ERR_TIMEOUT: return "a kernel's bounded wait ran out";

@@ -46,7 +46,7 @@ typedef enum {
   TTT_ERR_NULL = -1,        /* a required pointer is NULL */
   TTT_ERR_SHAPE = -2,       /* sizes inconsistent (e.g. N % chunk != 0) */
   TTT_ERR_ALIGN = -3,       /* a pointer is not 16-byte aligned */
-  TTT_ERR_UNSUPPORTED = -4, /* valid request this build does not implement */
+  TTT_ERR_UNSUPPORTED = -4, /* valid request the library does not implement */
   TTT_ERR_WORKSPACE = -5,   /* workspace NULL or smaller than the query says */
   TTT_ERR_CUDA = -6,        /* a CUDA runtime call failed (no device, launch) */
   TTT_ERR_TIMEOUT = -7,     /* a kernel's bounded wait ran out (device word) */
