@@ -410,7 +410,8 @@ __global__ void __launch_bounds__(kHThreads, 1)
       const int rl = q * 32 + lane;
       const int grow = r * 128 + rl;                  // row inside the matrix
       const int qc = half / 2;                        // columns per thread
-      const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c2 * qc);
+      const uint32_t tlb = tmem + ((uint32_t)(q * 32) << 16);       // this warp's TMEM lanes
+      const uint32_t tl = tlb + (uint32_t)(c2 * qc);
       const bool leader = e_warp == 0 && lane == 0;
       const float ca = L.a, cb = L.b, cc = L.c;
       const uint32_t a_saddr = smem_u32(apanel);
@@ -424,23 +425,24 @@ __global__ void __launch_bounds__(kHThreads, 1)
           half_update(L, z, r, h, rl, c2, e_warp, lane, tl, sc, got, rs_own, rs_peer, apanel, wbar,
                       rsbar, peer_rs, peer_rsbar);
         } else {
-          if (got) {
-            for (int c0 = 0; c0 < qc; c0 += 32) {
-              const int gcol = h * half + c2 * qc + c0;
-              half_block(kind, ca, cb, cc, sc, tl + c0,
-                         a_saddr + (gcol >> 6) * kHChunk + rl * 128, rl, grow, gcol);
-            }
+          // The half panel is drained one 64-column chunk at a time (each
+          // warp takes 32 columns of it); G and X', which the other CTAs read
+          // as B operands, leave chunk by chunk by TMA store as soon as every
+          // warp has written the chunk, under the drain of the next ones.
+          const int map = kind == 0 ? HM_G_P : (((tp + 1) & 1) ? HM_X1_P : HM_X0_P);
+#pragma unroll
+          for (int j = 0; j < R; ++j) {
+            const int lc = 64 * j + 32 * c2;   // column inside this CTA's half
+            if (got)
+              half_block(kind, ca, cb, cc, sc, tlb + (uint32_t)lc,
+                         a_saddr + (h * R + j) * kHChunk + rl * 128, rl, grow, h * half + lc);
+            fence_proxy_async_smem();
+            named_bar_sync(1, 256);
+            if (leader && got && kind != 1)
+              tma_store_2d(&L.maps[map], (h * R + j) * 64, prow, apanel + (h * R + j) * kHChunk);
           }
-          fence_proxy_async_smem();
-          named_bar_sync(1, 256);
           if (leader && got) {
-            if (kind != 1) {   // G and X' are read by the other CTAs as B operands
-              const int map = kind == 0 ? HM_G_P : (((tp + 1) & 1) ? HM_X1_P : HM_X0_P);
-              for (int j = 0; j < R; ++j)
-                tma_store_2d(&L.maps[map], (h * R + j) * 64, prow,
-                             apanel + (h * R + j) * kHChunk);
-              bulk_commit_group();
-            }
+            if (kind != 1) bulk_commit_group();
             // This half of the panel goes to the partner, completing on its panel
             // barrier.  Before a cluster barrier (G, X') the copy is issued after
             // the barrier arrival: a release-ordered arrival would wait for it.
