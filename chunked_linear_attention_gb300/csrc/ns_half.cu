@@ -207,17 +207,27 @@ __device__ __noinline__ void half_update(const NsHalfLaunch& L, int z, int r, in
     bulk_commit_group();
   }
   if (okw) {   // bf16 operand copy: warp e_warp writes rows 16 e_warp .. + 15 of the block
+    // lane l converts columns 8 l .. 8 l + 7 (two 16-byte shared loads, one
+    // 16-byte store); four rows are in flight per iteration
     __nv_bfloat16* Wb = static_cast<__nv_bfloat16*>(L.Wb[slot]) + (long long)wrow * d + wcol;
-    const int sub = lane >> 3, u = lane & 7;
-    for (int rr = e_warp * 16; rr < e_warp * 16 + 16; ++rr) {
-      for (int c4 = 0; c4 < nwc; c4 += 4) {
-        const int ch = c4 + sub;
-        if (ch < nwc) {
-          const uint4 w =
-              lds128(wsaddr + ch * 16384 + rr * 128 + ((uint32_t)(u ^ (rr & 7)) << 4));
-          const uint2 o = make_uint2(hpack(__uint_as_float(w.x), __uint_as_float(w.y)),
-                                     hpack(__uint_as_float(w.z), __uint_as_float(w.w)));
-          *reinterpret_cast<uint2*>(Wb + (long long)rr * d + ch * 32 + u * 4) = o;
+    const int ch = lane >> 2, g = 2 * (lane & 3);
+    if (lane < half / 8) {
+      for (int r0 = e_warp * 16; r0 < e_warp * 16 + 16; r0 += 4) {
+        uint4 w0[4], w1[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int rr = r0 + i;
+          const uint32_t row = wsaddr + ch * 16384 + rr * 128;
+          w0[i] = lds128(row + ((uint32_t)(g ^ (rr & 7)) << 4));
+          w1[i] = lds128(row + ((uint32_t)((g + 1) ^ (rr & 7)) << 4));
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 o = make_uint4(hpack(__uint_as_float(w0[i].x), __uint_as_float(w0[i].y)),
+                                     hpack(__uint_as_float(w0[i].z), __uint_as_float(w0[i].w)),
+                                     hpack(__uint_as_float(w1[i].x), __uint_as_float(w1[i].y)),
+                                     hpack(__uint_as_float(w1[i].z), __uint_as_float(w1[i].w)));
+          *reinterpret_cast<uint4*>(Wb + (long long)(r0 + i) * d + 8 * lane) = o;
         }
       }
     }
