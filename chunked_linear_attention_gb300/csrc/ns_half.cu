@@ -49,6 +49,7 @@ namespace {
 constexpr int kHThreads = 320;
 constexpr int kHCtrl = 3072;                 // barriers, TMEM slot, row sums (own [2][128], peer [128])
 constexpr int kHMaxStages = 8;
+constexpr int kHMaxR = 4;                    // largest order d = 128 kHMaxR
 constexpr int kHChunk = 128 * 64 * 2;        // one 64-column chunk of a 128-row bf16 panel
 constexpr int kHProdLanes = 1;               // TMA-issuing lanes of warp 0 (2 measured no faster)
 
@@ -248,14 +249,16 @@ __global__ void __launch_bounds__(kHThreads, 1)
   uint64_t* empty = full + kHMaxStages;
   uint64_t* mma_done = empty + kHMaxStages;   // both partners' MMAs of a product complete
   uint64_t* own_ready = mma_done + 1;         // this CTA's half of the next A panel written
-  uint64_t* pready = own_ready + 1;           // the partner's half landed (bulk copy bytes)
-  uint64_t* abar = pready + 1;                // first A panel loaded
+  uint64_t* pready = own_ready + 1;           // [R] chunk j of the partner's half landed
+  uint64_t* abar = pready + kHMaxR;           // first A panel loaded
   uint64_t* wbar = abar + 1;                  // fp32 W block loaded (final update)
   uint64_t* rsbar = wbar + 1;                 // partner's row sums written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rsbar + 1);
   float* rs_own = reinterpret_cast<float*>(smem + 1024);   // [2][128]
   float* rs_peer = rs_own + 256;                           // [128], written by the partner
   static_assert(1024 + 3 * 128 * 4 <= kHCtrl, "row sums inside the control region");
+  static_assert(R <= kHMaxR && (2 * kHMaxStages + kHMaxR + 6) * 8 + 4 <= 1024,
+                "barriers and TMEM slot below the row sums");
   uint8_t* apanel = smem + kHCtrl;
 
   constexpr int d = 128 * R, nk = d / 64, half = d / 2;
@@ -279,7 +282,7 @@ __global__ void __launch_bounds__(kHThreads, 1)
     }
     mbar_init(mma_done, 2);
     mbar_init(own_ready, 1);
-    mbar_init(pready, 1);
+    for (int j = 0; j < R; ++j) mbar_init(&pready[j], 1);
     mbar_init(abar, 1);
     mbar_init(wbar, 1);
     mbar_init(rsbar, 1);
@@ -298,7 +301,7 @@ __global__ void __launch_bounds__(kHThreads, 1)
   // every warp sums the partials in the same fixed order (same value everywhere)
   const float s1 =
       1.0f / (sqrtf(sum_partials_warp(L.normsq_part + (long long)z * L.nslot, L.nslot)) + L.eps);
-  const uint32_t peer_pready = map_cluster(smem_u32(pready), (uint32_t)partner);
+  const uint32_t peer_pready = map_cluster(smem_u32(pready), (uint32_t)partner);   // + 8 j: chunk j
   const uint32_t peer_panel = map_cluster(smem_u32(apanel), (uint32_t)partner);
   const uint32_t peer_rs = map_cluster(smem_u32(rs_peer), (uint32_t)partner);
   const uint32_t peer_rsbar = map_cluster(smem_u32(rsbar), (uint32_t)partner);
@@ -387,8 +390,8 @@ __global__ void __launch_bounds__(kHThreads, 1)
           const uint32_t bkk = kind == 2 ? 2048 / 16 : 32 / 16;
           for (int i = 0; i < nk; ++i) {
             const int ks = i < R ? h * R + i : (1 - h) * R + i - R;
-            if (i == R && p > 0) {
-              if (!mbar_wait_cluster_w(pready, (uint32_t)((p - 1) & 1), L.status, lim)) {
+            if (i >= R && p > 0) {   // chunk i - R of the partner's half
+              if (!mbar_wait_cluster_w(&pready[i - R], (uint32_t)((p - 1) & 1), L.status, lim)) {
                 ok = false;
                 break;
               }
@@ -438,7 +441,9 @@ __global__ void __launch_bounds__(kHThreads, 1)
           // The half panel is drained one 64-column chunk at a time (each
           // warp takes 32 columns of it); G and X', which the other CTAs read
           // as B operands, leave chunk by chunk by TMA store as soon as every
-          // warp has written the chunk, under the drain of the next ones.
+          // warp has written the chunk, under the drain of the next ones.  P
+          // needs no store; each chunk goes straight to the partner instead,
+          // landing on that chunk's own barrier there.
           const int map = kind == 0 ? HM_G_P : (((tp + 1) & 1) ? HM_X1_P : HM_X0_P);
 #pragma unroll
           for (int j = 0; j < R; ++j) {
@@ -448,23 +453,22 @@ __global__ void __launch_bounds__(kHThreads, 1)
                          a_saddr + (h * R + j) * kHChunk + rl * 128, rl, grow, h * half + lc);
             fence_proxy_async_smem();
             named_bar_sync(1, 256);
-            if (leader && got && kind != 1)
-              tma_store_2d(&L.maps[map], (h * R + j) * 64, prow, apanel + (h * R + j) * kHChunk);
+            if (leader && got) {
+              const uint32_t off = (uint32_t)((h * R + j) * kHChunk);
+              if (kind != 1)
+                tma_store_2d(&L.maps[map], (h * R + j) * 64, prow, apanel + off);
+              else
+                bulk_copy_s2c(peer_panel + off, a_saddr + off, (uint32_t)kHChunk,
+                              peer_pready + 8u * (uint32_t)j);
+            }
           }
           if (leader && got) {
             if (kind != 1) bulk_commit_group();
-            // This half of the panel goes to the partner, completing on its panel
-            // barrier.  Before a cluster barrier (G, X') the copy is issued after
-            // the barrier arrival: a release-ordered arrival would wait for it.
-            if (kind == 1) {
-              for (int j = 0; j < R; ++j) {
-                const uint32_t off = (uint32_t)((h * R + j) * kHChunk);
-                bulk_copy_s2c(peer_panel + off, a_saddr + off, (uint32_t)kHChunk, peer_pready);
-              }
-            } else {
-              copy_after_arrive = true;
-            }
-            mbar_arrive_expect_tx(pready, (uint32_t)(R * kHChunk));
+            // Before a cluster barrier (G, X') the copies to the partner are
+            // issued after the barrier arrival: a release-ordered arrival would
+            // wait for them.
+            if (kind != 1) copy_after_arrive = true;
+            for (int j = 0; j < R; ++j) mbar_arrive_expect_tx(&pready[j], (uint32_t)kHChunk);
             mbar_arrive(own_ready);
             if (kind != 1) {
               bulk_wait_all();
@@ -480,7 +484,8 @@ __global__ void __launch_bounds__(kHThreads, 1)
       if (copy_after_arrive) {
         for (int j = 0; j < R; ++j) {
           const uint32_t off = (uint32_t)((h * R + j) * kHChunk);
-          bulk_copy_s2c(peer_panel + off, smem_u32(apanel) + off, (uint32_t)kHChunk, peer_pready);
+          bulk_copy_s2c(peer_panel + off, smem_u32(apanel) + off, (uint32_t)kHChunk,
+                        peer_pready + 8u * (uint32_t)j);
         }
         copy_after_arrive = false;
       }
