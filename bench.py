@@ -599,6 +599,8 @@ def run_ours(args):
         cla.ttt_layer_forward_host(hq, hk, hv, heta, hW1, hW2, hW3, b, wl.mode, step.rule,
                                    update_chunks=wl.update_chunks, out=h_out, W_final=h_W,
                                    workspace=ws_host)
+        # the step's result is read on the host: wait for the call to complete
+        stream.synchronize()
 
     e2e_steps = max(1, min(args.steps, 20))
     ms_e2e = time_steps(torch, e2e_step, e2e_steps, 3, stream)
