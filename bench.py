@@ -15,8 +15,9 @@ m768, 8 chunks of 8192, update on chunks 0-3) and the million-token context
 (B1 H4 d=m=512, N = 1,048,576, chunk 8192, Muon 5) under "workloads";
 ``--workload`` makes either of them the headline instead.
 
-The library is single-GPU: its Newton-Schulz kernels use TMA multicast
-within a thread-block cluster, which is kept to one-GPU jobs.  A launch on
+The library is single-GPU: the layer runs on one GPU without sharding
+(the (batch, head) sequences shard only as independent replicas, and no
+replica mode is provided).  A launch on
 more than one GPU (``--gpus N`` with N > 1, or torchrun with WORLD_SIZE > 1)
 prints one line saying so and exits 0 without touching a GPU.
 ``--impl reference`` times the fp64 CPU oracle instead, on a bounded sample of
@@ -61,9 +62,9 @@ def single_gpu_refusal(args):
         return None
     return {"metric": METRIC, "value": None, "unit": UNIT, "n_gpus": n, "steps": args.steps,
             "warmup": args.warmup, "higher_is_better": True,
-            "unavailable": "single-GPU build: the Newton-Schulz kernels use TMA cluster multicast, "
-                           "which is kept to one-GPU jobs; the layer shards only as independent "
-                           "replicas and no replica mode is provided"}
+            "unavailable": "single-GPU build: the layer runs on one GPU without sharding; its "
+                           "(batch, head) sequences shard only as independent replicas and no "
+                           "replica mode is provided"}
 
 
 # ---------------------------------------------------------------------------

@@ -107,18 +107,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-// The same box delivered to every CTA of the cluster named in `cta_mask`, at
-// this CTA's shared-memory offset `smem_dst`, completing on the barrier at
-// this CTA's offset `bar` in each destination CTA.
-__device__ __forceinline__ void tma_load_2d_mc(void* smem_dst, const CUtensorMap* map, int x, int y,
-                                               uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask)
-      : "memory");
-}
-
 // 3-D tiled load of one box into this CTA's shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, int x, int y,
                                             int w, uint64_t* bar) {
@@ -126,17 +114,6 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(w), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// 3-D tiled load of one box, multicast to the CTAs in `cta_mask`.
-__device__ __forceinline__ void tma_load_3d_mc(void* smem_dst, const CUtensorMap* map, int x, int y,
-                                               int w, uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(w), "r"(smem_u32(bar)),
-      "h"(cta_mask)
       : "memory");
 }
 
